@@ -1,0 +1,44 @@
+"""CPU oracle for the FP8 block-scaled GEMM family.  TEST INFRASTRUCTURE ONLY.
+
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may import
+this package.  The library (the CUDA kernels behind the C ABI) never calls it,
+and it shares no code with the library: no kernels, headers, tables, helpers or
+constants.
+
+What it computes is the plain definition of each operation, slow and in
+float64, so that it can be checked against the pages by eye:
+
+  * E4M3 decode (closed form of the 8-bit "fn" format) and UE8M0 decode
+    (2**(b - 127)): the DeepGEMM README, "Interface / Notes", which names E4M3
+    operands and UE8M0 scale factors (linking the PTX "alternate floating point
+    data formats" section).
+  * the scale-factor pack: four UE8M0 bytes per int32, MN-major, MN extent
+    padded to 16 bytes (README "Interface / Notes": "4 UE8M0 packed into one
+    torch.int", transposed, TMA-aligned; README "Utilities":
+    get_mn_major_tma_aligned_packed_ue8m0_tensor, get_tma_aligned_size; the
+    DeepGEMM-Ascend news article, "Cómo funciona", packs scale pairs along K in
+    MN-major order).
+  * D = A @ B^T with fine-grained scales (README "Interface / Notes": fp8_gemm_nt
+    computes D = C + A @ B.T; the article's §四.2 gemm_fp8_fp8_bf16_nt takes lhs,
+    rhs, lhs_scale, rhs_scale and returns BF16).
+  * the M-grouped contiguous and masked layouts (README "Grouped GEMM
+    (contiguous layout)" and "Grouped GEMM (masked layout)"; the article's §五.1
+    layout table).
+
+Readings where the pages are silent (each listed in the design notes):
+  P2  byte j of packed word kp holds K block 4*kp + j (little-endian).
+  P3  B's 128x128 scales are broadcast to one packed word per row of B.
+  P4  MN padded to a multiple of 4 int32 (16 bytes) with zero words.
+  P5  a scale that is not a power of two rounds UP to the next one; below
+      2**-127 gives byte 0x00, above 2**127 gives 0xFE; zero, negative, NaN or
+      Inf gives 0xFF.  This convention is parity UNPINNED by the pages.
+  P7  the exact sum is rounded once to BF16, round-to-nearest-even.
+  P8  contiguous-layout padding rows (m_indices == -1) come out as +0.0.
+  P9  masked-layout rows at or past masked_m[g] keep whatever D held before.
+"""
+from .reference import (  # noqa: F401
+    e4m3_decode_table, e4m3_decode, ue8m0_decode, ue8m0_encode, tma_aligned_size,
+    pack_sf_ue8m0, unpack_sf_ue8m0, bf16_round_bits, bf16_bits_to_float,
+    fp8_gemm_nt, fp8_gemm_nt_unrounded, m_grouped_fp8_gemm_nt_contiguous,
+    m_grouped_fp8_gemm_nt_masked,
+)

@@ -1,0 +1,258 @@
+"""Plain float64 definitions of the FP8 block-scaled GEMM family (test infrastructure).
+
+See the package docstring for the passages each function follows and for the
+readings taken where the pages are silent.  Nothing here is tuned: every
+function is the definition written out, with numpy's matmul as the one library
+step (used only where the result is exact, see `_block_products`).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+BLOCK_K = 128        # scale granularity along K (1x128 for A, 128x128 for B)
+
+
+# ---------------------------------------------------------------------------
+# Formats (README "Interface / Notes": E4M3 operands, UE8M0 scale factors)
+# ---------------------------------------------------------------------------
+
+def _e4m3_value(code: int) -> float:
+    """The 8-bit E4M3 ("fn") value of one code: sign, 4 exponent bits (bias 7), 3 mantissa bits.
+
+    Exponent field 0 is subnormal, (m/8) * 2**-6.  Exponent field 15 with mantissa 7 is NaN
+    (the format has no infinity); all other codes are normal, (1 + m/8) * 2**(e - 7).
+    """
+    s = (code >> 7) & 1
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return math.nan
+    if e == 0:
+        mag = (m / 8.0) * 2.0 ** -6
+    else:
+        mag = (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return -mag if s else mag
+
+
+def e4m3_decode_table() -> np.ndarray:
+    """float64[256]: the value of every E4M3 code."""
+    return np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+_E4M3 = e4m3_decode_table()
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    return _E4M3[np.asarray(codes, dtype=np.uint8)]
+
+
+def ue8m0_decode(b) -> np.ndarray:
+    """UE8M0 byte -> 2**(b - 127); 0xFF is NaN."""
+    b = np.asarray(b, dtype=np.int64)
+    out = np.ldexp(1.0, b - 127)
+    return np.where(b == 0xFF, np.nan, out)
+
+
+def ue8m0_encode(x) -> np.ndarray:
+    """Float scales -> UE8M0 bytes (reading P5), elementwise.
+
+    The byte is the smallest b in 0..254 with 2**(b - 127) >= x, or 0xFE when x > 2**127.
+    Zero, negative, NaN and infinite x give 0xFF.  With x = f * 2**fe (f in [0.5, 1)):
+    x is the power 2**(fe - 1) when f == 0.5, otherwise the next power up is 2**fe.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    bad = ~(x > 0.0) | np.isinf(x)
+    f, fe = np.frexp(np.where(bad, 1.0, x))
+    b = fe.astype(np.int64) + 127 - (f == 0.5)
+    b = np.clip(b, 0, 0xFE)
+    return np.where(bad, 0xFF, b).astype(np.uint8)
+
+
+def tma_aligned_size(mn: int, elem_bytes: int = 4) -> int:
+    """MN rounded up so that one MN-major row of the scale tensor spans a multiple of 16 bytes
+    (README "Utilities": get_tma_aligned_size)."""
+    per = 16 // elem_bytes
+    return (mn + per - 1) // per * per
+
+
+# ---------------------------------------------------------------------------
+# Scale-factor pack (README "Interface / Notes" and "Utilities"; Ascend article, "Cómo funciona")
+# ---------------------------------------------------------------------------
+
+def pack_sf_ue8m0(sf: np.ndarray, mn: int, gran_mn: int) -> np.ndarray:
+    """float sf[G][ceil(mn/gran_mn)][Kb] -> int32 [G][ceil(Kb/4)][tma_aligned_size(mn)].
+
+    Word [g][kp][r] holds, in byte j (bits 8j..8j+7), the UE8M0 code of the scale covering
+    row r and K block 4*kp + j: sf[g][r // gran_mn][4*kp + j].  Bytes for K blocks past Kb,
+    and whole words for rows r >= mn, are zero.
+    """
+    sf = np.asarray(sf, dtype=np.float32)
+    if sf.ndim == 2:
+        sf = sf[None]
+    G, MNb, Kb = sf.shape
+    assert MNb == (mn + gran_mn - 1) // gran_mn
+    Kp = (Kb + 3) // 4
+    codes = ue8m0_encode(sf)                                  # [G, MNb, Kb]
+    per_row = codes[:, np.arange(mn) // gran_mn, :]           # [G, mn, Kb]: scale of row r
+    padded = np.zeros((G, mn, 4 * Kp), dtype=np.uint32)       # K blocks past Kb stay 0
+    padded[:, :, :Kb] = per_row
+    bytes4 = padded.reshape(G, mn, Kp, 4)
+    words = (bytes4[..., 0] | (bytes4[..., 1] << 8) | (bytes4[..., 2] << 16)
+             | (bytes4[..., 3] << 24))                        # [G, mn, Kp]
+    out = np.zeros((G, Kp, tma_aligned_size(mn, 4)), dtype=np.uint32)
+    out[:, :, :mn] = words.transpose(0, 2, 1)                 # MN-major; rows >= mn stay 0
+    return out.view(np.int32)
+
+
+def unpack_sf_ue8m0(packed: np.ndarray, mn: int, kb_count: int) -> np.ndarray:
+    """int32 [G][Kp][al4(mn)] -> uint8 codes [G][mn][Kb]: the inverse view of the pack."""
+    p = np.asarray(packed).view(np.uint32)
+    if p.ndim == 2:
+        p = p[None]
+    G, Kp, _ = p.shape
+    codes = np.zeros((G, mn, kb_count), dtype=np.uint8)
+    for kb in range(kb_count):
+        kp, j = divmod(kb, 4)
+        codes[:, :, kb] = (p[:, kp, :mn] >> (8 * j)) & 0xFF
+    return codes
+
+
+# ---------------------------------------------------------------------------
+# BF16 rounding (reading P7)
+# ---------------------------------------------------------------------------
+
+def bf16_round_bits(x: np.ndarray) -> np.ndarray:
+    """float64 -> BF16 bit patterns (uint16), one round-to-nearest-even step.
+
+    BF16 has 8 significant bits and FP32's exponent range: normal binades 2**-126 ..
+    2**127, subnormal spacing 2**-133.  The quantum of x is 2**(max(E, -126) - 7) with E
+    the binade exponent of x; x / quantum is exact, np.rint rounds it half-to-even, and the
+    product is exactly representable in BF16 (hence in float32, whose top 16 bits it is).
+    Results of magnitude >= 2**128 are infinities.  NaN maps to 0x7FC0.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    nan = np.isnan(x)
+    _, fe = np.frexp(np.where(nan, 0.0, x))           # |x| in [2**(fe-1), 2**fe)
+    E = fe.astype(np.int64) - 1
+    q_exp = np.maximum(E, -126) - 7
+    with np.errstate(over="ignore", invalid="ignore"):
+        r = np.rint(np.ldexp(np.where(nan, 0.0, x), -q_exp))
+        y = np.ldexp(r, q_exp)
+    inf = np.abs(y) >= 2.0 ** 128
+    y32 = np.where(inf, 0.0, y).astype(np.float32)   # exact: y is a BF16 value
+    bits = (y32.view(np.uint32) >> 16).astype(np.uint16)
+    bits = np.where(inf, np.where(y > 0, 0x7F80, 0xFF80), bits).astype(np.uint16)
+    bits = np.where(nan, 0x7FC0, bits).astype(np.uint16)
+    out[...] = bits
+    return out
+
+
+def bf16_bits_to_float(bits: np.ndarray) -> np.ndarray:
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# GEMMs (README "Interface / Notes", "Grouped GEMM (contiguous / masked layout)")
+# ---------------------------------------------------------------------------
+
+def _block_products(a_codes: np.ndarray, b_codes: np.ndarray, kb: int) -> np.ndarray:
+    """sum_{k in block kb} e4m3(A[m,k]) * e4m3(B[n,k]) for all m, n, exactly.
+
+    Every E4M3 value is an integer multiple of 2**-9 below 2**9, so each product is a
+    multiple of 2**-18 below 2**18 and a 128-term sum needs fewer than 43 bits: float64
+    holds it exactly in any summation order, which is why a library matmul may be used.
+    """
+    ks = slice(kb * BLOCK_K, (kb + 1) * BLOCK_K)
+    a = e4m3_decode(a_codes[:, ks])
+    b = e4m3_decode(b_codes[:, ks])
+    return a @ b.T
+
+
+def fp8_gemm_nt_unrounded(a_codes, sfa_packed, b_codes, sfb_packed) -> np.ndarray:
+    """float64 D[m, n] = sum_kb 2**(sa(m,kb)-127) * 2**(sb(n,kb)-127) * sum_{k in kb} a*b.
+
+    a_codes uint8 [M, K], b_codes uint8 [N, K]; sfa_packed int32 [Kp][al4(M)] and
+    sfb_packed int32 [Kp][al4(N)] are packed UE8M0 words (one per row).  The K blocks are
+    added in ascending order; each block's sum is exact (see `_block_products`).
+    """
+    a_codes = np.asarray(a_codes, dtype=np.uint8)
+    b_codes = np.asarray(b_codes, dtype=np.uint8)
+    M, K = a_codes.shape
+    N = b_codes.shape[0]
+    assert K % BLOCK_K == 0 and b_codes.shape[1] == K
+    Kb = K // BLOCK_K
+    sa = unpack_sf_ue8m0(sfa_packed, M, Kb)[0]        # [M, Kb] codes
+    sb = unpack_sf_ue8m0(sfb_packed, N, Kb)[0]        # [N, Kb]
+    d = np.zeros((M, N), dtype=np.float64)
+    for kb in range(Kb):
+        scale = ue8m0_decode(sa[:, kb])[:, None] * ue8m0_decode(sb[:, kb])[None, :]
+        d += scale * _block_products(a_codes, b_codes, kb)
+    return d
+
+
+def fp8_gemm_nt(a_codes, sfa_packed, b_codes, sfb_packed) -> np.ndarray:
+    """BF16 bits [M, N] of D = A @ B^T (dense; the definition above, rounded once)."""
+    return bf16_round_bits(fp8_gemm_nt_unrounded(a_codes, sfa_packed, b_codes, sfb_packed))
+
+
+def m_grouped_fp8_gemm_nt_contiguous(a_codes, sfa_packed, b_codes, sfb_packed, m_indices,
+                                     rows=None) -> np.ndarray:
+    """BF16 bits [M_sum, N] of the contiguous-layout grouped GEMM.
+
+    Row m with e = m_indices[m] >= 0 is the dense row A[m] @ B[e]^T with A's scales and
+    expert e's scales; rows with m_indices[m] == -1 are +0.0 (reading P8).
+    a_codes [M_sum, K]; sfa_packed [Kp][al4(M_sum)]; b_codes [G, N, K];
+    sfb_packed [G][Kp][al4(N)].  `rows` restricts the computation to a subset of rows
+    (the result then has len(rows) rows, in that order).
+    """
+    a_codes = np.asarray(a_codes, dtype=np.uint8)
+    m_indices = np.asarray(m_indices, dtype=np.int64)
+    M_sum, K = a_codes.shape
+    G, N, _ = b_codes.shape
+    Kb = K // BLOCK_K
+    rows = np.arange(M_sum) if rows is None else np.asarray(rows, dtype=np.int64)
+    sa_all = unpack_sf_ue8m0(sfa_packed, M_sum, Kb)[0]
+    out = np.zeros((rows.size, N), dtype=np.uint16)
+    for e in range(G):
+        sel = np.nonzero(m_indices[rows] == e)[0]
+        if sel.size == 0:
+            continue
+        r = rows[sel]
+        sub_sfa = _repack_rows(sa_all[r])
+        out[sel] = fp8_gemm_nt(a_codes[r], sub_sfa, b_codes[e], sfb_packed[e])
+    return out
+
+
+def m_grouped_fp8_gemm_nt_masked(a_codes, sfa_packed, b_codes, sfb_packed, masked_m,
+                                 d_prior) -> np.ndarray:
+    """BF16 bits [G, max_m, N] of the masked-layout grouped GEMM.
+
+    For every group g, rows m < masked_m[g] are the dense rows A[g][m] @ B[g]^T; all other
+    rows keep the bits of d_prior (reading P9).
+    """
+    a_codes = np.asarray(a_codes, dtype=np.uint8)
+    G, max_m, K = a_codes.shape
+    out = np.array(d_prior, dtype=np.uint16, copy=True)
+    Kb = K // BLOCK_K
+    for g in range(G):
+        m = int(masked_m[g])
+        if m <= 0:
+            continue
+        sa = unpack_sf_ue8m0(sfa_packed[g], max_m, Kb)[0][:m]
+        out[g, :m] = fp8_gemm_nt(a_codes[g, :m], _repack_rows(sa), b_codes[g], sfb_packed[g])
+    return out
+
+
+def _repack_rows(codes_rows: np.ndarray) -> np.ndarray:
+    """uint8 codes [R, Kb] -> packed int32 [Kp][al4(R)] (the pack layout, for a row subset)."""
+    R, Kb = codes_rows.shape
+    Kp = (Kb + 3) // 4
+    out = np.zeros((Kp, tma_aligned_size(R, 4)), dtype=np.uint32)
+    for kb in range(Kb):
+        kp, j = divmod(kb, 4)
+        out[kp, :R] |= codes_rows[:, kb].astype(np.uint32) << (8 * j)
+    return out.view(np.int32)
