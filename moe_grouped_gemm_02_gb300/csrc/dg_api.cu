@@ -1,0 +1,382 @@
+// The C ABI: host-side argument checks, kernel-configuration choice, TMA descriptor
+// encoding and launches.  Everything here runs on the host; the arithmetic is in the
+// kernels (dg_gemm_kernel.cuh, dg_pack.cu).
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "dg.h"
+#include "dg_internal.h"
+
+namespace dg {
+
+// Set by a GEMM kernel whose barrier wait timed out; read and cleared by dg_check_device_error.
+__device__ int g_device_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxMaskedGroups = 4096;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;   // 4 s per barrier wait
+
+struct DeviceState {
+    bool init = false;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    int* err_ptr = nullptr;
+    int max_smem = 0;   // opt-in dynamic shared memory per block
+    bool prepared = false;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+int g_num_sms_cap = -1;   // -1: not read from the environment yet
+
+const KernelConfig* const* all_configs(int* n) {
+    static const KernelConfig* cfgs[] = {&config_bn256_s4_a1(), &config_bn224_s4_a2(), &config_bn128_s6_a2(),
+                                         &config_bn64_s8_a2(), &config_bn32_s8_a2()};
+    *n = static_cast<int>(sizeof(cfgs) / sizeof(cfgs[0]));
+    return cfgs;
+}
+
+bool env_flag(const char* name) {
+    const char* v = std::getenv(name);
+    return v && v[0] && std::strcmp(v, "0") != 0;
+}
+
+// DG_ERR_CUDA, with the failing call printed when DG_PRINT_CONFIGS is set.
+dg_status cuda_fail(const char* what, cudaError_t e) {
+    if (env_flag("DG_PRINT_CONFIGS"))
+        std::fprintf(stderr, "[dg] %s failed: %s\n", what, cudaGetErrorString(e));
+    return DG_ERR_CUDA;
+}
+
+int sms_cap_locked() {
+    if (g_num_sms_cap < 0) {
+        const char* v = std::getenv("DG_NUM_SMS");
+        g_num_sms_cap = v ? std::atoi(v) : 0;
+        if (g_num_sms_cap < 0) g_num_sms_cap = 0;
+    }
+    return g_num_sms_cap;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Current device's state; initialises it (attributes, error-word address, kernel attributes)
+// on first use.
+dg_status current_device(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DG_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.init) {
+        cudaError_t e;
+        if ((e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&st.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&st.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&st.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+            return cuda_fail("cudaDeviceGetAttribute", e);
+        st.init = true;
+    }
+    if (st.cc_major != 10 || st.cc_minor != 3) return DG_ERR_UNSUPPORTED_DEVICE;
+    if (!st.prepared) {
+        cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&st.err_ptr), g_device_error_word);
+        if (e != cudaSuccess) return cuda_fail("cudaGetSymbolAddress", e);
+        int n = 0;
+        const KernelConfig* const* cfgs = all_configs(&n);
+        for (int i = 0; i < n; ++i)
+            if ((e = cfgs[i]->prepare(st.max_smem)) != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", e);
+        st.prepared = true;
+    }
+    *out = &st;
+    return DG_OK;
+}
+
+int effective_sms(const DeviceState& st) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const int cap = sms_cap_locked();
+    return (cap > 0 && cap < st.sm_count) ? cap : st.sm_count;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int al4(int x) { return (x + 3) / 4 * 4; }
+
+bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, uint64_t elem_bytes, const void* ptr, uint64_t d0,
+               uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, CUtensorMapSwizzle swz) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * elem_bytes, d0 * d1 * elem_bytes};
+    cuuint32_t box[3] = {b0, b1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Configuration choice: estimated time ~ waves * (per-tile cost), per-tile cost growing with
+// BN plus a fixed overhead; the single-accumulator configuration pays for its unoverlapped
+// epilogue.
+const KernelConfig* choose_config(int m_blocks_total, int N, int sms) {
+    int n = 0;
+    const KernelConfig* const* cfgs = all_configs(&n);
+    const KernelConfig* best = nullptr;
+    double best_cost = 0;
+    for (int i = 0; i < n; ++i) {
+        const KernelConfig* c = cfgs[i];
+        const long long tiles = static_cast<long long>(m_blocks_total) * ((N + c->bn - 1) / c->bn);
+        const long long waves = (tiles + sms - 1) / sms;
+        const double cost = static_cast<double>(waves) * (c->bn * (c->acc == 1 ? 1.06 : 1.0) + 16.0);
+        if (!best || cost < best_cost) {
+            best = c;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+dg_status run_gemm(int mode, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, void* d,
+                   const int32_t* m_indices, const int32_t* masked_m, int groups, int b_groups, int rows, int N,
+                   int K, void* stream) {
+    DeviceState* st = nullptr;
+    dg_status s = current_device(&st);
+    if (s != DG_OK) return s;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+    if (env_flag("DG_VALIDATE")) {
+        if (cudaStreamSynchronize(cs) != cudaSuccess) return cuda_fail("cudaStreamSynchronize", cudaGetLastError());
+        if (mode == MODE_CONTIGUOUS) {
+            std::vector<int32_t> h(static_cast<size_t>(rows));
+            if (cudaMemcpy(h.data(), m_indices, h.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+                return DG_ERR_CUDA;
+            // Per 128-row block: either all -1, or a run of one expert e followed by -1s.
+            // An expert's blocks are consecutive, and only the last of them may hold -1s.
+            std::vector<char> seen(static_cast<size_t>(b_groups), 0);
+            int prev_e = -1;
+            bool prev_full = false;
+            for (int blk = 0; blk < rows / 128; ++blk) {
+                const int e = h[static_cast<size_t>(blk) * 128];
+                if (e < -1 || e >= b_groups) return DG_ERR_CONTRACT;
+                int n_valid = 0;
+                bool pad = false;
+                for (int r = blk * 128; r < blk * 128 + 128; ++r) {
+                    const int x = h[r];
+                    if (e >= 0 && x == e && !pad) ++n_valid;
+                    else if (x == -1) pad = true;
+                    else return DG_ERR_CONTRACT;
+                }
+                if (e == -1) {
+                    prev_e = -1;
+                    prev_full = false;
+                    continue;
+                }
+                if (e == prev_e) {
+                    if (!prev_full) return DG_ERR_CONTRACT;
+                } else {
+                    if (seen[e]) return DG_ERR_CONTRACT;
+                    seen[e] = 1;
+                }
+                prev_e = e;
+                prev_full = n_valid == 128;
+            }
+        } else if (mode == MODE_MASKED) {
+            std::vector<int32_t> h(static_cast<size_t>(groups));
+            if (cudaMemcpy(h.data(), masked_m, h.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+                return DG_ERR_CUDA;
+            for (int g = 0; g < groups; ++g)
+                if (h[g] < 0 || h[g] > rows) return DG_ERR_CONTRACT;
+        }
+    }
+
+    const int sms = effective_sms(*st);
+    const int m_blocks = (rows + 127) / 128;
+    const KernelConfig* cfg = choose_config(m_blocks * groups, N, sms);
+    const int Kb = K / 128, Kp = (Kb + 3) / 4;
+
+    CUtensorMap maps[4];
+    const int a_groups = mode == MODE_MASKED ? groups : 1;
+    if (!encode_3d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, K, rows, a_groups, 128, 128,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, K, N, b_groups, 128, cfg->bn,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfa, al4(rows), Kp, a_groups, 128, 1,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_3d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfb, al4(N), Kp, b_groups, cfg->bn, 1,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+
+    GemmArgs args{};
+    args.rows = rows;
+    args.N = N;
+    args.K = K;
+    args.mode = mode;
+    args.groups = groups;
+    args.b_groups = b_groups;
+    args.num_m_blocks = m_blocks;
+    args.num_n_blocks = (N + cfg->bn - 1) / cfg->bn;
+    args.kblocks = Kb;
+    args.m_indices = m_indices;
+    args.masked_m = masked_m;
+    args.d = static_cast<uint16_t*>(d);
+    args.err = st->err_ptr;
+    args.timeout_ns = kTimeoutNs;
+    long long units_upper = static_cast<long long>(m_blocks) * groups * args.num_n_blocks;
+    if (mode == MODE_CONTIGUOUS) {
+        args.raster_n = args.num_n_blocks;
+    } else {
+        args.raster_n = m_blocks >= 16 ? (args.num_n_blocks < 8 ? args.num_n_blocks : 8) : args.num_n_blocks;
+    }
+    args.num_units = mode == MODE_MASKED ? 0 : static_cast<int>(units_upper);
+    const int grid = static_cast<int>(units_upper < sms ? units_upper : sms);
+    if (env_flag("DG_PRINT_CONFIGS"))
+        std::fprintf(stderr, "[dg] mode=%d groups=%d rows=%d N=%d K=%d -> %s (BN=%d stages=%d acc=%d) grid=%d raster_n=%d\n",
+                     mode, groups, rows, N, K, cfg->name, cfg->bn, cfg->stages, cfg->acc, grid, args.raster_n);
+    if (grid <= 0) return DG_OK;
+    if (cfg->smem_bytes(mode == MODE_MASKED ? groups + 1 : 0) > static_cast<size_t>(st->max_smem)) return DG_ERR_SHAPE;
+    const cudaError_t e = cfg->launch(maps, args, grid, cs);
+    return e == cudaSuccess ? DG_OK : cuda_fail("kernel launch", e);
+}
+
+dg_status check_common(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const void* d,
+                       int N, int K) {
+    if (!a || !sfa || !b || !sfb || !d) return DG_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0) return DG_ERR_INVALID_ARG;
+    if (K % 128 != 0 || N % 8 != 0) return DG_ERR_SHAPE;
+    if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(d))
+        return DG_ERR_ALIGNMENT;
+    return DG_OK;
+}
+
+}  // namespace
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" {
+
+dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, void* d, int M,
+                         int N, int K, void* stream) {
+    if (M < 0) return DG_ERR_INVALID_ARG;
+    const dg_status s = check_common(a, sfa, b, sfb, d, N, K);
+    if (s != DG_OK) return s;
+    if (static_cast<long long>(M) * K >= (1ll << 40) || static_cast<long long>(N) * K >= (1ll << 40))
+        return DG_ERR_SHAPE;
+    if (M == 0) return DG_OK;
+    return run_gemm(MODE_DENSE, a, sfa, b, sfb, d, nullptr, nullptr, 1, 1, M, N, K, stream);
+}
+
+dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                              void* d, const int32_t* m_indices, int M_sum, int N, int K, int G,
+                                              void* stream) {
+    if (M_sum < 0 || G <= 0 || !m_indices) return DG_ERR_INVALID_ARG;
+    const dg_status s = check_common(a, sfa, b, sfb, d, N, K);
+    if (s != DG_OK) return s;
+    if (M_sum % 128 != 0) return DG_ERR_SHAPE;
+    if (static_cast<long long>(M_sum) * K >= (1ll << 40) || static_cast<long long>(G) * N * K >= (1ll << 40))
+        return DG_ERR_SHAPE;
+    if (M_sum == 0) return DG_OK;
+    return run_gemm(MODE_CONTIGUOUS, a, sfa, b, sfb, d, m_indices, nullptr, 1, G, M_sum, N, K, stream);
+}
+
+dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                          void* d, const int32_t* masked_m, int G, int max_m, int N, int K,
+                                          void* stream) {
+    if (max_m < 0 || G <= 0 || !masked_m) return DG_ERR_INVALID_ARG;
+    if (G > kMaxMaskedGroups) return DG_ERR_SHAPE;
+    const dg_status s = check_common(a, sfa, b, sfb, d, N, K);
+    if (s != DG_OK) return s;
+    if (static_cast<long long>(G) * max_m * K >= (1ll << 40) || static_cast<long long>(G) * N * K >= (1ll << 40))
+        return DG_ERR_SHAPE;
+    if (max_m == 0) return DG_OK;
+    return run_gemm(MODE_MASKED, a, sfa, b, sfb, d, nullptr, masked_m, G, G, max_m, N, K, stream);
+}
+
+dg_status dg_pack_sf_ue8m0(const float* sf, int32_t* out, int G, int MN, int K, int gran_mn, int gran_k,
+                           void* stream) {
+    if (!sf || !out || G <= 0 || MN < 0 || K <= 0) return DG_ERR_INVALID_ARG;
+    if (gran_mn != 1 && gran_mn != 128) return DG_ERR_INVALID_ARG;
+    if (gran_k != 128) return DG_ERR_INVALID_ARG;
+    if (K % 128 != 0) return DG_ERR_SHAPE;
+    if (!aligned16(out) || (reinterpret_cast<uintptr_t>(sf) & 3u)) return DG_ERR_ALIGNMENT;
+    const int Kb = K / 128, Kp = (Kb + 3) / 4;
+    if (Kp > 65535 || G > 65535) return DG_ERR_SHAPE;
+    if (MN == 0) return DG_OK;
+    DeviceState* st = nullptr;
+    const dg_status s = current_device(&st);
+    if (s != DG_OK) return s;
+    const int MNb = (MN + gran_mn - 1) / gran_mn;
+    const cudaError_t e = launch_pack_sf(sf, out, G, MN, MNb, Kb, Kp, al4(MN), gran_mn,
+                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
+int dg_get_mk_alignment_for_contiguous_layout(void) { return 128; }
+
+int dg_get_tma_aligned_size(int mn, int elem_bytes) {
+    if (mn < 0 || !(elem_bytes == 1 || elem_bytes == 2 || elem_bytes == 4 || elem_bytes == 8 || elem_bytes == 16))
+        return -1;
+    const int per = 16 / elem_bytes;
+    return (mn + per - 1) / per * per;
+}
+
+void dg_set_num_sms(int n) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_num_sms_cap = n > 0 ? n : 0;
+}
+
+int dg_get_num_sms(void) {
+    DeviceState* st = nullptr;
+    if (current_device(&st) != DG_OK) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        return sms_cap_locked();
+    }
+    return effective_sms(*st);
+}
+
+const char* dg_status_string(dg_status s) {
+    switch (s) {
+        case DG_OK: return "ok";
+        case DG_ERR_INVALID_ARG: return "invalid argument";
+        case DG_ERR_SHAPE: return "unsupported shape";
+        case DG_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+        case DG_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3";
+        case DG_ERR_CUDA: return "CUDA error";
+        case DG_ERR_TIMEOUT: return "kernel barrier wait timed out";
+        case DG_ERR_CONTRACT: return "m_indices / masked_m violate the layout contract";
+    }
+    return "unknown status";
+}
+
+dg_status dg_check_device_error(void* stream) {
+    DeviceState* st = nullptr;
+    const dg_status s = current_device(&st);
+    if (s != DG_OK) return s;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DG_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, st->err_ptr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DG_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(st->err_ptr, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return DG_ERR_CUDA;
+        if (env_flag("DG_PRINT_CONFIGS")) std::fprintf(stderr, "[dg] device error word 0x%x\n", word);
+        return DG_ERR_TIMEOUT;
+    }
+    return DG_OK;
+}
+
+}  // extern "C"

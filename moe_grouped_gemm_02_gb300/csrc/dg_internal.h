@@ -1,0 +1,57 @@
+// Types shared between the host dispatcher and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dg {
+
+enum : int { MODE_DENSE = 0, MODE_CONTIGUOUS = 1, MODE_MASKED = 2 };
+
+// Timeout sites recorded in the device error word (bits 8..15), DG_ERR_TIMEOUT in bits 0..7.
+enum : int { SITE_EMPTY = 1, SITE_FULL = 2, SITE_TMEM_EMPTY = 3, SITE_TMEM_FULL = 4, SITE_DRAIN = 5 };
+
+struct GemmArgs {
+    int rows;           // rows of A and D per group: M (dense), M_sum (contiguous), max_m (masked)
+    int N, K;
+    int mode;           // MODE_*
+    int groups;         // groups of A and D (masked: G; otherwise 1)
+    int b_groups;       // groups of B (dense: 1; contiguous and masked: G)
+    int num_m_blocks;   // ceil(rows / 128)
+    int num_n_blocks;   // ceil(N / BN)
+    int kblocks;        // K / 128
+    int raster_n;       // n-blocks per raster band (dense and contiguous)
+    int num_units;      // tiles to compute (dense and contiguous); masked counts on the device
+    const int32_t* m_indices;
+    const int32_t* masked_m;
+    uint16_t* d;        // BF16 bit patterns
+    int* err;           // device error word
+    unsigned long long timeout_ns;
+};
+
+using GemmLaunchFn = cudaError_t (*)(const CUtensorMap* maps, const GemmArgs& args, int grid,
+                                     cudaStream_t stream);
+
+struct KernelConfig {
+    int bn;             // N tile (columns of D per tile)
+    int stages;         // shared-memory pipeline depth
+    int acc;            // TMEM accumulator buffers
+    const char* name;
+    size_t (*smem_bytes)(int extra_ints);
+    GemmLaunchFn launch;
+    cudaError_t (*prepare)(int max_smem);   // per-device one-time kernel attribute setup
+};
+
+// One per instantiation translation unit.
+const KernelConfig& config_bn256_s4_a1();
+const KernelConfig& config_bn224_s4_a2();
+const KernelConfig& config_bn128_s6_a2();
+const KernelConfig& config_bn64_s8_a2();
+const KernelConfig& config_bn32_s8_a2();
+
+cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb, int Kb, int Kp,
+                           int mn_al, int gran_mn, cudaStream_t stream);
+
+}  // namespace dg
