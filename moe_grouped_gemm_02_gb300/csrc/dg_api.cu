@@ -30,6 +30,7 @@ struct DeviceState {
     int* err_ptr = nullptr;
     int max_smem = 0;   // opt-in dynamic shared memory per block
     bool prepared = false;
+    int clusters[16][3] = {};   // co-resident clusters per configuration for split 2 and 4 (0: unknown)
 };
 
 std::mutex g_mu;
@@ -37,8 +38,9 @@ DeviceState g_dev[kMaxDevices];
 int g_num_sms_cap = -1;   // -1: not read from the environment yet
 
 const KernelConfig* const* all_configs(int* n) {
-    static const KernelConfig* cfgs[] = {&config_bn256_s4_a1(), &config_bn224_s4_a2(), &config_bn128_s6_a2(),
-                                         &config_bn64_s8_a2(), &config_bn32_s8_a2()};
+    static const KernelConfig* cfgs[] = {&config_bn256_s4_a1(), &config_bn224_s4_a2(),
+                                         &config_bn192_s5_a2(), &config_bn128_s6_a2(), &config_bn128_s4_a2(), &config_bn64_s8_a2(),
+                                         &config_bn32_s8_a2()};
     *n = static_cast<int>(sizeof(cfgs) / sizeof(cfgs[0]));
     return cfgs;
 }
@@ -130,24 +132,61 @@ bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, uint64_t elem_bytes, cons
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Configuration choice: estimated time ~ waves * (per-tile cost), per-tile cost growing with
-// BN plus a fixed overhead; the single-accumulator configuration pays for its unoverlapped
-// epilogue.
-const KernelConfig* choose_config(int m_blocks_total, int N, int sms) {
+// Plan choice: a kernel configuration and a split-K factor.  The estimate, from GB300
+// measurements, is waves * (K blocks per CTA * t_kb(BN) + t_tile + t_reduce), where a K block
+// costs about 600 + 1.2 * BN cycles in the main loop, a tile about 3000 cycles of fixed cost
+// (pipeline fill and epilogue), and a split-K reduction through distributed shared memory
+// about 1500 cycles.  Waves count tiles per co-resident CTA (or cluster of `split` CTAs).
+struct Plan {
+    const KernelConfig* cfg = nullptr;
+    int split = 1;
+    int capacity = 0;   // co-resident CTAs (split 1) or clusters (split > 1)
+};
+
+int cluster_capacity(DeviceState& st, int cfg_index, const KernelConfig* c, int split, int extra_ints) {
+    const int si = split == 2 ? 1 : 2;
+    std::lock_guard<std::mutex> lk(g_mu);
+    int& v = st.clusters[cfg_index][si];
+    if (v == 0) {
+        v = c->max_clusters(split, c->smem_bytes(extra_ints, split));
+        if (v <= 0) v = -1;
+    }
+    return v;
+}
+
+Plan choose_plan(DeviceState& st, int mode, int m_blocks_total, int N, int kblocks, int sms, int extra_ints) {
     int n = 0;
     const KernelConfig* const* cfgs = all_configs(&n);
-    const KernelConfig* best = nullptr;
+    const int ngroups = (kblocks + 3) / 4;
+    // DG_FORCE_CONFIG=<name> and DG_FORCE_SPLIT=<1|2|4> pin the plan, for tuning sweeps.
+    const char* force_cfg = std::getenv("DG_FORCE_CONFIG");
+    const char* force_split = std::getenv("DG_FORCE_SPLIT");
+    const int fsplit = force_split ? std::atoi(force_split) : 0;
+    Plan best;
     double best_cost = 0;
     for (int i = 0; i < n; ++i) {
         const KernelConfig* c = cfgs[i];
-        const long long tiles = static_cast<long long>(m_blocks_total) * ((N + c->bn - 1) / c->bn);
-        const long long waves = (tiles + sms - 1) / sms;
-        const double cost = static_cast<double>(waves) * (c->bn * (c->acc == 1 ? 1.06 : 1.0) + 16.0);
-        if (!best || cost < best_cost) {
-            best = c;
-            best_cost = cost;
+        if (force_cfg && std::strcmp(force_cfg, c->name) != 0) continue;
+        for (int split : {1, 2, 4}) {
+            if (fsplit && split != fsplit) continue;
+            if (split > 1 && (ngroups < split || c->bn % 32 != 0)) continue;
+            if (c->smem_bytes(extra_ints, split) > static_cast<size_t>(st.max_smem)) continue;
+            const int cap = split == 1 ? sms : std::min(cluster_capacity(st, i, c, split, extra_ints), sms / split);
+            if (cap <= 0) continue;
+            const long long tiles = static_cast<long long>(m_blocks_total) * ((N + c->bn - 1) / c->bn);
+            const long long waves = (tiles + cap - 1) / cap;
+            const double kb_per = 4.0 * ((ngroups + split - 1) / split);
+            const double t_tile = kb_per * (600.0 + 1.2 * c->bn) + 3000.0 + (split > 1 ? 1500.0 : 0.0);
+            const double cost = static_cast<double>(waves) * t_tile;
+            if (!best.cfg || cost < best_cost - 1e-9) {
+                best.cfg = c;
+                best.split = split;
+                best.capacity = cap;
+                best_cost = cost;
+            }
         }
     }
+    (void)mode;
     return best;
 }
 
@@ -206,8 +245,11 @@ dg_status run_gemm(int mode, const void* a, const int32_t* sfa, const void* b, c
 
     const int sms = effective_sms(*st);
     const int m_blocks = (rows + 127) / 128;
-    const KernelConfig* cfg = choose_config(m_blocks * groups, N, sms);
     const int Kb = K / 128, Kp = (Kb + 3) / 4;
+    const int extra_ints = mode == MODE_MASKED ? groups + 1 : 0;
+    const Plan plan = choose_plan(*st, mode, m_blocks * groups, N, Kb, sms, extra_ints);
+    if (!plan.cfg) return DG_ERR_SHAPE;   // nothing fits in shared memory (too many masked groups)
+    const KernelConfig* cfg = plan.cfg;
 
     CUtensorMap maps[4];
     const int a_groups = mode == MODE_MASKED ? groups : 1;
@@ -243,12 +285,17 @@ dg_status run_gemm(int mode, const void* a, const int32_t* sfa, const void* b, c
         args.raster_n = m_blocks >= 16 ? (args.num_n_blocks < 8 ? args.num_n_blocks : 8) : args.num_n_blocks;
     }
     args.num_units = mode == MODE_MASKED ? 0 : static_cast<int>(units_upper);
-    const int grid = static_cast<int>(units_upper < sms ? units_upper : sms);
+    args.split = plan.split;
+    // Persistent grid: one CTA (or one cluster of `split` CTAs) per co-resident slot.
+    const long long slots = units_upper < plan.capacity ? units_upper : plan.capacity;
+    const int grid = static_cast<int>(slots) * plan.split;
     if (env_flag("DG_PRINT_CONFIGS"))
-        std::fprintf(stderr, "[dg] mode=%d groups=%d rows=%d N=%d K=%d -> %s (BN=%d stages=%d acc=%d) grid=%d raster_n=%d\n",
-                     mode, groups, rows, N, K, cfg->name, cfg->bn, cfg->stages, cfg->acc, grid, args.raster_n);
+        std::fprintf(stderr,
+                     "[dg] mode=%d groups=%d rows=%d N=%d K=%d -> %s (BN=%d stages=%d acc=%d) split=%d grid=%d "
+                     "raster_n=%d\n",
+                     mode, groups, rows, N, K, cfg->name, cfg->bn, cfg->stages, cfg->acc, plan.split, grid,
+                     args.raster_n);
     if (grid <= 0) return DG_OK;
-    if (cfg->smem_bytes(mode == MODE_MASKED ? groups + 1 : 0) > static_cast<size_t>(st->max_smem)) return DG_ERR_SHAPE;
     const cudaError_t e = cfg->launch(maps, args, grid, cs);
     return e == cudaSuccess ? DG_OK : cuda_fail("kernel launch", e);
 }

@@ -35,7 +35,8 @@ namespace dg {
 constexpr int BM = 128;       // rows per tile: the tcgen05 M
 constexpr int BK = 128;       // K per stage: one 128-byte swizzle row, one scale block
 constexpr int MMA_K = 32;     // K of one kind::mxf8f6f4 MMA
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;
+constexpr uint32_t SF_WARP = 6;     // warp that re-lays scale words for tcgen05.cp
 constexpr int DG_ERR_TIMEOUT_CODE = 6;
 
 template <int BN_, int STAGES_, int ACC_>
@@ -43,17 +44,21 @@ struct GemmCfg {
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
     static constexpr int ACC = ACC_;
-    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
+    static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 16 in [32, 256]");
+    static_assert(ACC == 1 || BN % 32 == 0, "a second accumulator must start on a 32-column boundary");
     static constexpr int SFB_CHUNKS = (BN + 127) / 128;   // 128-row scale chunks of a B tile
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int SFA_BYTES = 512;
     static constexpr int SFB_BYTES = SFB_CHUNKS * 512;
-    static constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + BM * 4 + BN * 4;
-    // TMEM columns: ACC accumulators of BN columns, then per stage 4 columns of A scales
-    // and 4 per 128-row chunk of B scales.
+    static constexpr uint32_t TX_AB = A_BYTES + B_BYTES;
+    static constexpr uint32_t TX_SF = BM * 4 + BN * 4;
+    // The packed scale words of a group of four K blocks travel in their own ring of SF_SLOTS
+    // slots (shared memory, then TMEM): TMEM columns are ACC accumulators of BN columns, then
+    // per slot 4 columns of A scales and 4 per 128-row chunk of B scales.
     static constexpr int SF_COLS = 4 + 4 * SFB_CHUNKS;
-    static constexpr int TMEM_USED = ACC * BN + STAGES * SF_COLS;
+    static constexpr int SF_SLOTS = 3;
+    static constexpr int TMEM_USED = ACC * BN + SF_SLOTS * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64
                                    : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
@@ -61,13 +66,24 @@ struct GemmCfg {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC;
+    static constexpr int OFF_SFB = OFF_SFA + SF_SLOTS * SFA_BYTES;
+    static constexpr int OFF_BAR = OFF_SFB + SF_SLOTS * SFB_BYTES;
+    // full/empty per stage; tmem full/empty per accumulator; sf full/ready/empty per scale
+    // slot; split-K reduce: 4 full, 1 empty.
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 3 * SF_SLOTS + 5;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
     static constexpr int OFF_CUM = OFF_MISC + 16;             // masked mode: m-block prefix sums
-    static size_t smem_bytes(int extra_ints) {
-        return 1024 + OFF_CUM + static_cast<size_t>(extra_ints) * 4;
+    // Split-K receive buffer: for every quadrant of rows this CTA owns (4 / split of them), one
+    // slot per other CTA of the cluster, 32 rows of BN FP32 (rows padded by 16 bytes).
+    static constexpr int RECV_ROW = BN * 4 + 16;
+    static __host__ __device__ uint32_t off_recv(int extra_ints) {
+        return (static_cast<uint32_t>(OFF_CUM + extra_ints * 4) + 15u) & ~15u;
+    }
+    static __host__ __device__ uint32_t recv_bytes(int split) {
+        return split > 1 ? static_cast<uint32_t>((4 / split) * (split - 1) * 32 * RECV_ROW) : 0u;
+    }
+    static size_t smem_bytes(int extra_ints, int split) {
+        return 1024 + off_recv(extra_ints) + recv_bytes(split);
     }
 };
 
@@ -134,6 +150,29 @@ static __device__ __noinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     }
 }
 
+// Same, acquiring at cluster scope: for barriers completed by other CTAs of the cluster.
+static __device__ __noinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                                   int* err, unsigned long long timeout_ns, int site) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > timeout_ns) {
+            *abort_flag = 1u;
+            if (err) atomicCAS(err, 0, DG_ERR_TIMEOUT_CODE | (site << 8));
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, int* err,
+                                          unsigned long long timeout_ns, int site) {
+    return mbar_try_wait(bar, parity) || wait_or_abort(bar, parity, abort_flag, err, timeout_ns, site);
+}
+
 // Re-lay one 128-row chunk of scale words (word r = row r, as TMA landed it) into the layout
 // tcgen05.cp.32x128b.warpx4 expects: the 16 bytes at offset 16*i hold rows i, i+32, i+64,
 // i+96.  Whole warp; in place.
@@ -172,6 +211,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto empty_bar = [&](int s) { return base + C::OFF_BAR + 8u * (C::STAGES + s); };
     auto tfull_bar = [&](int a) { return base + C::OFF_BAR + 8u * (2 * C::STAGES + a); };
     auto tempty_bar = [&](int a) { return base + C::OFF_BAR + 8u * (2 * C::STAGES + C::ACC + a); };
+    constexpr int SFB0 = 2 * C::STAGES + 2 * C::ACC;   // first scale-ring barrier
+    auto sfempty_bar = [&](int j) { return base + C::OFF_BAR + 8u * (SFB0 + j); };
+    auto sfready_bar = [&](int j) { return base + C::OFF_BAR + 8u * (SFB0 + C::SF_SLOTS + j); };
+    auto sffull_bar = [&](int j) { return base + C::OFF_BAR + 8u * (SFB0 + 2 * C::SF_SLOTS + j); };
+    auto redfull_bar = [&](int j) { return base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + j); };
+    const uint32_t redempty_bar = base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + 4);
+    const int split = args.split;
+    const uint32_t recv_base = base + C::off_recv(args.mode == MODE_MASKED ? args.groups + 1 : 0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -182,6 +229,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), 4 * 32);
         }
+        for (int j = 0; j < C::SF_SLOTS; ++j) {
+            mbar_init(sfempty_bar(j), 1);
+            mbar_init(sfready_bar(j), 1);
+            mbar_init(sffull_bar(j), 1);
+        }
+        for (int j = 0; j < 4; ++j) mbar_init(redfull_bar(j), 1);
+        mbar_init(redempty_bar, split > 1 ? 4 - 4 / split : 1);
         misc[1] = 0u;
         fence_mbarrier_init();
     }
@@ -221,12 +275,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if (split > 1) cluster_sync_all();   // peers' barriers are initialised before any remote use
+    else __syncthreads();
     tc_fence_after_sync();
 
     const uint32_t tmem_base = misc[0];
+    // Split-K: the CTAs of a cluster take the same tiles; CTA `crank` covers K-block groups
+    // [crank * ngroups / split, (crank + 1) * ngroups / split) (groups of four K blocks).
+    const uint32_t crank = split > 1 ? cluster_ctarank() : 0u;
+    const int u_first = split > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int u_step = split > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+    const int ngroups = (args.kblocks + 3) / 4;
+    const int kb0 = 4 * (static_cast<int>(crank) * ngroups / split);
+    const int kb1 = min(args.kblocks, 4 * ((static_cast<int>(crank) + 1) * ngroups / split));
     const int total_units = args.mode == MODE_MASKED ? cum[args.groups] * args.num_n_blocks : args.num_units;
-    const int kblocks = args.kblocks;
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
@@ -234,22 +296,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0;   // stages issued in total (for the abort drain)
+            int sf_slot = 0;
+            uint32_t sf_phbits = 0;          // bit j: parity of scale slot j's empty barrier
+            int sf_last = -1;                // last scale slot loaded (for the abort drain)
+            uint32_t sf_last_par = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+            for (int u = u_first; ok && u < total_units; u += u_step) {
                 const Unit t = decode_unit(args, cum, u);
                 if (t.zero) continue;
                 const int ga = args.mode == MODE_MASKED ? t.g : 0;
-                for (int kb = 0; kb < kblocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if ((kb & 3) == 0) {
+                        // A new group of four K blocks: its packed scale words go to the next slot
+                        // of the scale ring once the MMAs of the slot's previous group are done.
+                        const uint32_t par = ((sf_phbits >> sf_slot) & 1u) ^ 1u;
+                        if (!wait_or_abort(sfempty_bar(sf_slot), par, misc + 1, args.err, args.timeout_ns,
+                                           SITE_SF_EMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                        sf_phbits ^= 1u << sf_slot;
+                        const uint32_t sb = sffull_bar(sf_slot);
+                        mbar_arrive_expect_tx(sb, C::TX_SF);
+                        tma_load_3d(base + C::OFF_SFA + sf_slot * C::SFA_BYTES, &tm_sfa, sb, t.mb * BM, kb >> 2, ga);
+                        tma_load_3d(base + C::OFF_SFB + sf_slot * C::SFB_BYTES, &tm_sfb, sb, t.nb * C::BN, kb >> 2,
+                                    t.gb);
+                        sf_last = sf_slot;
+                        sf_last_par = par ^ 1u;
+                        if (++sf_slot == C::SF_SLOTS) sf_slot = 0;
+                    }
                     if (!wait_or_abort(empty_bar(s), ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_EMPTY)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = full_bar(s);
-                    mbar_arrive_expect_tx(fb, C::TX_BYTES);
+                    mbar_arrive_expect_tx(fb, C::TX_AB);
                     tma_load_3d(base + C::OFF_A + s * C::A_BYTES, &tm_a, fb, kb * BK, t.mb * BM, ga);
                     tma_load_3d(base + C::OFF_B + s * C::B_BYTES, &tm_b, fb, kb * BK, t.nb * C::BN, t.gb);
-                    tma_load_3d(base + C::OFF_SFA + s * C::SFA_BYTES, &tm_sfa, fb, t.mb * BM, kb >> 2, ga);
-                    tma_load_3d(base + C::OFF_SFB + s * C::SFB_BYTES, &tm_sfb, fb, t.nb * C::BN, kb >> 2, t.gb);
                     ++issued;
                     if (++s == C::STAGES) { s = 0; ph ^= 1u; }
                 }
@@ -263,71 +346,121 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint64_t t0 = global_timer_ns();
                     while (!mbar_try_wait(full_bar(s), ph) && global_timer_ns() - t0 < 100000000ull) {}
                 }
+                if (sf_last >= 0) {
+                    const uint64_t t0 = global_timer_ns();
+                    while (!mbar_try_wait(sffull_bar(sf_last), sf_last_par) && global_timer_ns() - t0 < 100000000ull) {}
+                }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        int s = 0;
-        uint32_t ph = 0;
-        int acc = 0;
-        uint32_t acc_ph = 0;
-        bool ok = true;
-        bool any_commit = false;
-        uint32_t last_bar = 0, last_par = 0;
-        for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-            const Unit t = decode_unit(args, cum, u);
-            if (t.zero) continue;
-            if (!wait_or_abort(tempty_bar(acc), acc_ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_TMEM_EMPTY)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::BN);
-            for (int kb = 0; kb < kblocks; ++kb) {
-                if (!wait_or_abort(full_bar(s), ph, misc + 1, args.err, args.timeout_ns, SITE_FULL)) {
+        // One lane, a minimal loop: the issuing thread's instruction stream is on the critical
+        // path of the tensor pipe, so everything that can happen elsewhere does.
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t acc_ph = 0;
+            int sf_slot = 0;
+            uint32_t sfr_phbits = 0;   // bit j: parity of scale slot j's ready barrier
+            uint32_t sfa_t = 0, sfb_t = 0;
+            bool ok = true;
+            bool any_commit = false;
+            uint32_t last_bar = 0, last_par = 0;
+            const uint64_t adesc0 = smem_desc_kmajor_sw128(base + C::OFF_A);
+            const uint64_t bdesc0 = smem_desc_kmajor_sw128(base + C::OFF_B);
+            const uint32_t idesc0 = idesc_mxf8_e4m3(BM, C::BN, 0);
+            for (int u = u_first; ok && u < total_units; u += u_step) {
+                const Unit t = decode_unit(args, cum, u);
+                if (t.zero) continue;
+                if (!wait_fast(tempty_bar(acc), acc_ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_TMEM_EMPTY)) {
                     ok = false;
                     break;
                 }
-                uint32_t* sfa_w = reinterpret_cast<uint32_t*>(gbase + C::OFF_SFA + s * C::SFA_BYTES);
-                uint32_t* sfb_w = reinterpret_cast<uint32_t*>(gbase + C::OFF_SFB + s * C::SFB_BYTES);
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::BN);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if ((kb & 3) == 0) {
+                        // First K block of a group: copy the group's re-laid scale words from its
+                        // ring slot into the matching TMEM slot.  (The slot's previous MMAs are
+                        // complete: the producer waited for that before loading the slot.)
+                        if (!wait_fast(sfready_bar(sf_slot), (sfr_phbits >> sf_slot) & 1u, misc + 1, args.err,
+                                       args.timeout_ns, SITE_SF_READY)) {
+                            ok = false;
+                            break;
+                        }
+                        sfr_phbits ^= 1u << sf_slot;
+                        tc_fence_after_sync();
+                        sfa_t = tmem_base + static_cast<uint32_t>(C::ACC * C::BN + sf_slot * C::SF_COLS);
+                        sfb_t = sfa_t + 4u;
+                        tc_cp_32x128b_warpx4(sfa_t, smem_desc_sf_chunk(base + C::OFF_SFA + sf_slot * C::SFA_BYTES));
+#pragma unroll
+                        for (int c = 0; c < C::SFB_CHUNKS; ++c)
+                            tc_cp_32x128b_warpx4(sfb_t + 4u * c, smem_desc_sf_chunk(base + C::OFF_SFB +
+                                                                                    sf_slot * C::SFB_BYTES + 512 * c));
+                    }
+                    if (!wait_fast(full_bar(s), ph, misc + 1, args.err, args.timeout_ns, SITE_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t adesc = adesc0 + static_cast<uint64_t>((s * C::A_BYTES) >> 4);
+                    const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((s * C::B_BYTES) >> 4);
+                    const uint32_t sf_id = static_cast<uint32_t>(kb & 3);
+                    const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
+#pragma unroll
+                    for (int k = 0; k < BK / MMA_K; ++k)
+                        tc_mma_mxf8f6f4(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, sfa_t, sfb_t,
+                                        (kb != kb0 || k != 0) ? 1u : 0u);
+                    tc_commit(empty_bar(s));
+                    if ((kb & 3) == 3 || kb == kb1 - 1) {
+                        tc_commit(sfempty_bar(sf_slot));
+                        if (++sf_slot == C::SF_SLOTS) sf_slot = 0;
+                    }
+                    any_commit = true;
+                    last_bar = empty_bar(s);
+                    last_par = ph;
+                    if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(tfull_bar(acc));
+                if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
+            }
+            if ((!ok || misc[1]) && any_commit) {
+                // Abort: let the MMAs already issued finish before TMEM is freed.
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(last_bar, last_par) && global_timer_ns() - t0 < 100000000ull) {}
+            }
+        }
+    } else if (warp == SF_WARP) {
+        // ------------------------------------------------------------------ scale re-layout
+        // For every group of four K blocks, in order: wait for its scale words to land in their
+        // ring slot, re-lay them for tcgen05.cp, publish them to the async proxy and signal the
+        // MMA issuer.  Every party uses each slot's barriers once per group, in group order, so
+        // no wait is ever more than one phase from its barrier.
+        int sf_slot = 0;
+        uint32_t sff_phbits = 0;
+        bool ok = true;
+        for (int u = u_first; ok && u < total_units; u += u_step) {
+            const Unit t = decode_unit(args, cum, u);
+            if (t.zero) continue;
+            for (int kb = kb0; kb < kb1; kb += 4) {
+                if (!wait_fast(sffull_bar(sf_slot), (sff_phbits >> sf_slot) & 1u, misc + 1, args.err,
+                               args.timeout_ns, SITE_SF_FULL)) {
+                    ok = false;
+                    break;
+                }
+                sff_phbits ^= 1u << sf_slot;
+                uint32_t* sfa_w = reinterpret_cast<uint32_t*>(gbase + C::OFF_SFA + sf_slot * C::SFA_BYTES);
+                uint32_t* sfb_w = reinterpret_cast<uint32_t*>(gbase + C::OFF_SFB + sf_slot * C::SFB_BYTES);
                 relayout_sf_chunk(sfa_w, lane);
 #pragma unroll
                 for (int c = 0; c < C::SFB_CHUNKS; ++c) relayout_sf_chunk(sfb_w + 128 * c, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    tc_fence_after_sync();
-                    const uint32_t sfa_t = tmem_base + static_cast<uint32_t>(C::ACC * C::BN + s * C::SF_COLS);
-                    const uint32_t sfb_t = sfa_t + 4u;
-                    tc_cp_32x128b_warpx4(sfa_t, smem_desc_sf_chunk(base + C::OFF_SFA + s * C::SFA_BYTES));
-#pragma unroll
-                    for (int c = 0; c < C::SFB_CHUNKS; ++c)
-                        tc_cp_32x128b_warpx4(sfb_t + 4u * c,
-                                             smem_desc_sf_chunk(base + C::OFF_SFB + s * C::SFB_BYTES + 512 * c));
-                    const uint64_t adesc = smem_desc_kmajor_sw128(base + C::OFF_A + s * C::A_BYTES);
-                    const uint64_t bdesc = smem_desc_kmajor_sw128(base + C::OFF_B + s * C::B_BYTES);
-                    const uint32_t idesc = idesc_mxf8_e4m3(BM, C::BN, static_cast<uint32_t>(kb & 3));
-#pragma unroll
-                    for (int k = 0; k < BK / MMA_K; ++k)
-                        tc_mma_mxf8f6f4(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, sfa_t, sfb_t,
-                                        (kb | k) != 0 ? 1u : 0u);
-                    tc_commit(empty_bar(s));
-                }
-                __syncwarp();
-                any_commit = true;
-                last_bar = empty_bar(s);
-                last_par = ph;
-                if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+                if (lane == 0) mbar_arrive(sfready_bar(sf_slot));
+                if (++sf_slot == C::SF_SLOTS) sf_slot = 0;
             }
-            if (!ok) break;
-            if (lane == 0) tc_commit(tfull_bar(acc));
-            __syncwarp();
-            if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
-        }
-        if ((!ok || misc[1]) && any_commit) {
-            // Abort: let the MMAs already issued finish before TMEM is freed.
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(last_bar, last_par) && global_timer_ns() - t0 < 100000000ull) {}
         }
     } else {
         // ------------------------------------------------------------------ epilogue
@@ -336,7 +469,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int N = args.N;
         int acc = 0;
         uint32_t acc_ph = 0;
-        for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+        uint32_t red_ph = 0;   // split-K: parity of this warp's reduce barrier
+        for (int u = u_first; u < total_units; u += u_step) {
             if (misc[1]) break;
             const Unit t = decode_unit(args, cum, u);
             const int row = t.mb * BM + row_in_tile;
@@ -351,6 +485,97 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 write = row < m;
             }
             uint16_t* drow = args.d + (static_cast<size_t>(t.g) * args.rows + row) * static_cast<size_t>(N);
+            if (split > 1) {
+                // Reduce-scatter of the cluster's partial accumulators: quadrant q of the tile's
+                // rows belongs to CTA q / (4 / split); the others send it their partial rows.
+                const uint32_t qpc = 4u / static_cast<uint32_t>(split);
+                const uint32_t owner = q / qpc;
+                const uint32_t lq = q % qpc;
+                if (t.zero) {
+                    if (owner == crank && write)
+                        for (int c = n0; c < min(N, n0 + C::BN); c += 8) st_global_v4(drow + c, make_uint4(0, 0, 0, 0));
+                    continue;
+                }
+                if (!wait_or_abort(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
+                tc_fence_after_sync();
+                const uint32_t t_row = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * C::BN);
+                if (owner != crank) {
+                    if (!wait_cluster_or_abort(redempty_bar, red_ph ^ 1u, misc + 1, args.err, args.timeout_ns,
+                                               SITE_RED_EMPTY))
+                        break;
+                    red_ph ^= 1u;
+                    const uint32_t slot = crank < owner ? crank : crank - 1u;
+                    const uint32_t dst = map_to_rank(
+                        recv_base + ((lq * (split - 1) + slot) * 32u + lane) * C::RECV_ROW, owner);
+                    const uint32_t rbar = map_to_rank(redfull_bar(static_cast<int>(lq)), owner);
+#pragma unroll 1
+                    for (int c = 0; c < C::BN / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            st_async_v4(dst + 128u * c + 16u * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3], rbar);
+                    }
+                    tc_fence_before_sync();
+                    mbar_arrive(tempty_bar(acc));
+                } else {
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(redfull_bar(static_cast<int>(lq)),
+                                              static_cast<uint32_t>((split - 1) * 32 * C::BN * 4));
+                    if (!wait_cluster_or_abort(redfull_bar(static_cast<int>(lq)), red_ph, misc + 1, args.err,
+                                               args.timeout_ns, SITE_RED_FULL))
+                        break;
+                    red_ph ^= 1u;
+                    const uint32_t src = recv_base + (lq * (split - 1) * 32u + lane) * C::RECV_ROW;
+#pragma unroll 1
+                    for (int c = 0; c < C::BN / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                        tmem_wait_ld();
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                        for (int sl = 0; sl < split - 1; ++sl) {
+                            const float4* p = reinterpret_cast<const float4*>(
+                                gbase + (src - base) + static_cast<uint32_t>(sl) * 32u * C::RECV_ROW + 128u * c);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 x = p[j];
+                                v[4 * j] += x.x;
+                                v[4 * j + 1] += x.y;
+                                v[4 * j + 2] += x.z;
+                                v[4 * j + 3] += x.w;
+                            }
+                        }
+                        if (write) {
+                            const int col = n0 + 32 * c;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                if (col + 8 * j < N) {
+                                    uint4 o = make_uint4(0, 0, 0, 0);
+                                    if (!zero_row) {
+                                        o.x = pack_bf16x2(__float_as_uint(v[8 * j + 0]), __float_as_uint(v[8 * j + 1]));
+                                        o.y = pack_bf16x2(__float_as_uint(v[8 * j + 2]), __float_as_uint(v[8 * j + 3]));
+                                        o.z = pack_bf16x2(__float_as_uint(v[8 * j + 4]), __float_as_uint(v[8 * j + 5]));
+                                        o.w = pack_bf16x2(__float_as_uint(v[8 * j + 6]), __float_as_uint(v[8 * j + 7]));
+                                    }
+                                    st_global_v4(drow + col + 8 * j, o);
+                                }
+                            }
+                        }
+                    }
+                    tc_fence_before_sync();
+                    mbar_arrive(tempty_bar(acc));
+                    __syncwarp();
+                    if (lane == 0)
+                        for (int rk = 0; rk < split; ++rk)
+                            if (static_cast<uint32_t>(rk) != crank)
+                                mbar_arrive_remote(map_to_rank(redempty_bar, static_cast<uint32_t>(rk)));
+                }
+                if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
+                continue;
+            }
             if (t.zero) {
                 if (write)
                     for (int c = n0; c < min(N, n0 + C::BN); c += 8) st_global_v4(drow + c, make_uint4(0, 0, 0, 0));
@@ -360,15 +585,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after_sync();
             const uint32_t t_row = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * C::BN);
 #pragma unroll 1
-            for (int c = 0; c < C::BN / 32; ++c) {
+            for (int c = 0; c < (C::BN + 31) / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                const bool half = (C::BN % 32 != 0) && (c == C::BN / 32);   // 16-column tail chunk
+                if (half) tmem_ld_32x32b_x16(t_row + 32u * c, r);
+                else tmem_ld_32x32b_x32(t_row + 32u * c, r);
                 tmem_wait_ld();
                 if (write) {
                     const int col = n0 + 32 * c;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        if (col + 8 * j < N) {
+                        if (col + 8 * j < N && !(half && j >= 2)) {
                             uint4 v = make_uint4(0, 0, 0, 0);
                             if (!zero_row) {
                                 v.x = pack_bf16x2(r[8 * j + 0], r[8 * j + 1]);
@@ -388,7 +615,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    __syncwarp();
+    if (split > 1) cluster_sync_all();   // no CTA leaves while a peer may still touch its memory
+    else __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -398,9 +627,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 template <class C>
 cudaError_t launch_fp8_gemm(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStream_t stream) {
     const int extra = args.mode == MODE_MASKED ? args.groups + 1 : 0;
-    const size_t smem = C::smem_bytes(extra);
-    fp8_gemm_kernel<C><<<grid, NUM_THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], args);
-    return cudaGetLastError();
+    const size_t smem = C::smem_bytes(extra, args.split);
+    if (args.split <= 1) {
+        fp8_gemm_kernel<C><<<grid, NUM_THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], args);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(args.split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<C>, maps[0], maps[1], maps[2], maps[3], args);
+}
+
+template <class C>
+int max_clusters_fp8_gemm(int split, size_t smem) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(split), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel<C>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 template <class C>
@@ -412,7 +677,7 @@ cudaError_t prepare_fp8_gemm(int max_smem) {
     const KernelConfig& FN() {                                                                        \
         using C = GemmCfg<BN_, ST_, AC_>;                                                             \
         static const KernelConfig cfg{BN_, ST_, AC_, #FN, &C::smem_bytes, &launch_fp8_gemm<C>,        \
-                                      &prepare_fp8_gemm<C>};                                          \
+                                      &prepare_fp8_gemm<C>, &max_clusters_fp8_gemm<C>};               \
         return cfg;                                                                                   \
     }
 

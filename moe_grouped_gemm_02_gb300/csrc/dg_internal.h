@@ -11,7 +11,8 @@ namespace dg {
 enum : int { MODE_DENSE = 0, MODE_CONTIGUOUS = 1, MODE_MASKED = 2 };
 
 // Timeout sites recorded in the device error word (bits 8..15), DG_ERR_TIMEOUT in bits 0..7.
-enum : int { SITE_EMPTY = 1, SITE_FULL = 2, SITE_TMEM_EMPTY = 3, SITE_TMEM_FULL = 4, SITE_DRAIN = 5 };
+enum : int { SITE_EMPTY = 1, SITE_FULL = 2, SITE_TMEM_EMPTY = 3, SITE_TMEM_FULL = 4, SITE_SF_EMPTY = 5, SITE_RED_EMPTY = 6, SITE_RED_FULL = 7,
+             SITE_SF_READY = 8, SITE_SF_FULL = 9 };
 
 struct GemmArgs {
     int rows;           // rows of A and D per group: M (dense), M_sum (contiguous), max_m (masked)
@@ -24,6 +25,7 @@ struct GemmArgs {
     int kblocks;        // K / 128
     int raster_n;       // n-blocks per raster band (dense and contiguous)
     int num_units;      // tiles to compute (dense and contiguous); masked counts on the device
+    int split;          // CTAs (a thread-block cluster) sharing one tile's K range: 1, 2 or 4
     const int32_t* m_indices;
     const int32_t* masked_m;
     uint16_t* d;        // BF16 bit patterns
@@ -39,15 +41,18 @@ struct KernelConfig {
     int stages;         // shared-memory pipeline depth
     int acc;            // TMEM accumulator buffers
     const char* name;
-    size_t (*smem_bytes)(int extra_ints);
+    size_t (*smem_bytes)(int extra_ints, int split);
     GemmLaunchFn launch;
     cudaError_t (*prepare)(int max_smem);   // per-device one-time kernel attribute setup
+    int (*max_clusters)(int split, size_t smem);   // co-resident clusters of `split` CTAs
 };
 
 // One per instantiation translation unit.
 const KernelConfig& config_bn256_s4_a1();
 const KernelConfig& config_bn224_s4_a2();
+const KernelConfig& config_bn192_s5_a2();
 const KernelConfig& config_bn128_s6_a2();
+const KernelConfig& config_bn128_s4_a2();
 const KernelConfig& config_bn64_s8_a2();
 const KernelConfig& config_bn32_s8_a2();
 

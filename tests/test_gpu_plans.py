@@ -1,0 +1,104 @@
+"""Every kernel configuration and split-K factor, forced one at a time, against the oracle.
+
+The SM count is capped so that each persistent CTA (or cluster) walks many tiles: the
+pipeline, scale-ring and accumulator barriers then go through many phases, across tile
+boundaries, which is where ordering mistakes show.  Split-K runs the CTAs of a thread-block
+cluster over disjoint K ranges of one tile and reduces through distributed shared memory.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import moe_grouped_gemm_02_gb300 as dg
+from tests._parity import assert_within_tolerance, bits, to_dev
+
+pytestmark = pytest.mark.gpu
+
+CONFIGS = ["config_bn256_s4_a1", "config_bn224_s4_a2", "config_bn192_s5_a2", "config_bn128_s6_a2",
+           "config_bn128_s4_a2", "config_bn64_s8_a2", "config_bn32_s8_a2"]
+
+
+def _call_or_skip(fn, *args):
+    """A forced (configuration, split) pair that does not fit in shared memory is refused
+    with DG_ERR_SHAPE before launch; such pairs are never chosen by the planner."""
+    try:
+        fn(*args)
+    except dg.DGError as e:
+        if e.status == 2:
+            pytest.skip("forced plan does not fit in shared memory")
+        raise
+
+
+@pytest.fixture
+def few_sms():
+    dg.dg_set_num_sms(8)
+    yield
+    dg.dg_set_num_sms(0)
+
+
+def _dense(M, N, K, seed):
+    w = synth.make_dense(M, N, K, seed=seed, b_std=0.02)
+    sfa = oracle.pack_sf_ue8m0(w["sfa"], M, 1)[0]
+    sfb = oracle.pack_sf_ue8m0(w["sfb"], N, 128)[0]
+    return w, sfa, sfb, oracle.fp8_gemm_nt(w["a"], sfa, w["b"], sfb)
+
+
+@pytest.mark.parametrize("cfg", CONFIGS)
+@pytest.mark.parametrize("split", [1, 2, 4])
+def test_dense_every_plan(cfg, split, few_sms, monkeypatch):
+    monkeypatch.setenv("DG_FORCE_CONFIG", cfg)
+    monkeypatch.setenv("DG_FORCE_SPLIT", str(split))
+    M, N, K = 320, 704, 2560          # ragged M and N tails, 20 K blocks (5 groups of 4)
+    w, sfa, sfb, want = _dense(M, N, K, seed=len(cfg) + split)
+    d = torch.full((M, N), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
+    _call_or_skip(dg.dg_fp8_gemm_nt, to_dev(w["a"]), to_dev(sfa), to_dev(w["b"]), to_dev(sfb), d)
+    dg.dg_check_device_error()
+    assert_within_tolerance(bits(d), want, f"{cfg} split {split}")
+
+
+@pytest.mark.parametrize("split", [2, 4])
+def test_split_k_decode_shape(split, monkeypatch):
+    monkeypatch.setenv("DG_FORCE_SPLIT", str(split))
+    M, N, K = 64, 2112, 7168
+    w = synth.make_dense(M, N, K, seed=7, a_outliers=True, b_std=0.02)
+    sfa = oracle.pack_sf_ue8m0(w["sfa"], M, 1)[0]
+    sfb = oracle.pack_sf_ue8m0(w["sfb"], N, 128)[0]
+    d = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    dg.dg_fp8_gemm_nt(to_dev(w["a"]), to_dev(sfa), to_dev(w["b"]), to_dev(sfb), d)
+    dg.dg_check_device_error()
+    assert_within_tolerance(bits(d), oracle.fp8_gemm_nt(w["a"], sfa, w["b"], sfb), f"decode split {split}")
+
+
+@pytest.mark.parametrize("cfg", ["config_bn128_s6_a2", "config_bn128_s4_a2", "config_bn64_s8_a2"])
+@pytest.mark.parametrize("split", [1, 2, 4])
+def test_grouped_every_plan(cfg, split, few_sms, monkeypatch):
+    monkeypatch.setenv("DG_FORCE_CONFIG", cfg)
+    monkeypatch.setenv("DG_FORCE_SPLIT", str(split))
+    c = synth.make_contiguous(3, 256, 2048, tokens=0, seed=3, counts=[130, 0, 300])
+    csfa = oracle.pack_sf_ue8m0(c["sfa"], c["M_sum"], 1)[0]
+    csfb = oracle.pack_sf_ue8m0(c["sfb"], 256, 128)
+    d = torch.full((c["M_sum"], 256), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
+    _call_or_skip(dg.dg_m_grouped_fp8_gemm_nt_contiguous, to_dev(c["a"]), to_dev(csfa), to_dev(c["b"]),
+                  to_dev(csfb), d, to_dev(c["m_indices"]))
+    dg.dg_check_device_error()
+    got = bits(d)
+    valid = c["m_indices"] >= 0
+    assert np.all(got[~valid] == 0)
+    want = oracle.m_grouped_fp8_gemm_nt_contiguous(c["a"], csfa, c["b"], csfb, c["m_indices"])
+    assert_within_tolerance(got[valid], want[valid], f"contiguous {cfg} split {split}")
+
+    m = synth.make_masked(3, 200, 320, 2048, seed=4, masked_m=[199, 0, 129])
+    msfa = oracle.pack_sf_ue8m0(m["sfa"], 200, 1)
+    msfb = oracle.pack_sf_ue8m0(m["sfb"], 320, 128)
+    md = torch.full((3, 200, 320), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
+    dg.dg_m_grouped_fp8_gemm_nt_masked(to_dev(m["a"]), to_dev(msfa), to_dev(m["b"]), to_dev(msfb), md,
+                                      to_dev(m["masked_m"]))
+    dg.dg_check_device_error()
+    prior = np.full((3, 200, 320), synth.SENTINEL_BF16, np.uint16)
+    want = oracle.m_grouped_fp8_gemm_nt_masked(m["a"], msfa, m["b"], msfb, m["masked_m"], prior)
+    got = bits(md)
+    rows = np.arange(200)[None, :] < m["masked_m"][:, None]
+    assert np.array_equal(got[~rows], want[~rows])
+    assert_within_tolerance(got[rows], want[rows], f"masked {cfg} split {split}")
