@@ -30,7 +30,7 @@ struct DeviceState {
     int* err_ptr = nullptr;
     int max_smem = 0;   // opt-in dynamic shared memory per block
     bool prepared = false;
-    int clusters[16][3] = {};   // co-resident clusters per configuration for split 2 and 4 (0: unknown)
+    int clusters[16][4] = {};   // co-resident clusters per configuration: split 2, split 4, pair (0: unknown)
 };
 
 std::mutex g_mu;
@@ -40,7 +40,7 @@ int g_num_sms_cap = -1;   // -1: not read from the environment yet
 const KernelConfig* const* all_configs(int* n) {
     static const KernelConfig* cfgs[] = {&config_bn256_s4_a1(), &config_bn224_s4_a2(),
                                          &config_bn192_s5_a2(), &config_bn128_s6_a2(), &config_bn128_s4_a2(), &config_bn64_s8_a2(),
-                                         &config_bn32_s8_a2()};
+                                         &config_bn32_s8_a2(), &config_bn224_s3_m2(), &config_bn192_s3_m2()};
     *n = static_cast<int>(sizeof(cfgs) / sizeof(cfgs[0]));
     return cfgs;
 }
@@ -132,61 +132,81 @@ bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, uint64_t elem_bytes, cons
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Plan choice: a kernel configuration and a split-K factor.  The estimate, from GB300
-// measurements, is waves * (K blocks per CTA * t_kb(BN) + t_tile + t_reduce), where a K block
-// costs about 600 + 1.2 * BN cycles in the main loop, a tile about 3000 cycles of fixed cost
-// (pipeline fill and epilogue), and a split-K reduction through distributed shared memory
-// about 1500 cycles.  Waves count tiles per co-resident CTA (or cluster of `split` CTAs).
+// Plan choice: a kernel configuration, a split-K factor, and whether CTA pairs share B tiles by
+// multicast.  The estimate, from GB300 measurements, is waves * (K blocks per CTA * t_kb + t_tile
+// + t_reduce).  Per K block, an SM's TMA moves about one 128-byte row per 2.2 cycles (A: 128
+// rows, B: BN rows, or BN / 2 in pair mode) and a 128 x N x 32 MMA costs max(161, N / 2 + 33)
+// cycles (four per K block); t_kb is the larger.  A tile costs about 3000 cycles of fixed
+// work (pipeline fill, epilogue), a split-K reduction about 1500.  Waves count tiles per
+// co-resident CTA, cluster or pair.
 struct Plan {
     const KernelConfig* cfg = nullptr;
     int split = 1;
-    int capacity = 0;   // co-resident CTAs (split 1) or clusters (split > 1)
+    int pair = 0;
+    int capacity = 0;   // co-resident CTAs (plain) or clusters (split > 1, pair)
 };
 
-int cluster_capacity(DeviceState& st, int cfg_index, const KernelConfig* c, int split, int extra_ints) {
-    const int si = split == 2 ? 1 : 2;
+int cluster_capacity(DeviceState& st, int cfg_index, const KernelConfig* c, int cluster, int slot, int split,
+                     int extra_ints) {
     std::lock_guard<std::mutex> lk(g_mu);
-    int& v = st.clusters[cfg_index][si];
+    int& v = st.clusters[cfg_index][slot];
     if (v == 0) {
-        v = c->max_clusters(split, c->smem_bytes(extra_ints, split));
+        v = c->max_clusters(cluster, c->smem_bytes(extra_ints, split));
         if (v <= 0) v = -1;
     }
     return v;
 }
 
-Plan choose_plan(DeviceState& st, int mode, int m_blocks_total, int N, int kblocks, int sms, int extra_ints) {
+Plan choose_plan(DeviceState& st, int m_blocks_total, int N, int kblocks, int sms, int extra_ints) {
     int n = 0;
     const KernelConfig* const* cfgs = all_configs(&n);
     const int ngroups = (kblocks + 3) / 4;
-    // DG_FORCE_CONFIG=<name> and DG_FORCE_SPLIT=<1|2|4> pin the plan, for tuning sweeps.
+    // DG_FORCE_CONFIG=<name>, DG_FORCE_SPLIT=<1|2|4>, DG_FORCE_PAIR=<0|1> pin the plan (tuning).
     const char* force_cfg = std::getenv("DG_FORCE_CONFIG");
     const char* force_split = std::getenv("DG_FORCE_SPLIT");
+    const char* force_pair = std::getenv("DG_FORCE_PAIR");
     const int fsplit = force_split ? std::atoi(force_split) : 0;
+    const int fpair = force_pair ? std::atoi(force_pair) : -1;
     Plan best;
     double best_cost = 0;
     for (int i = 0; i < n; ++i) {
         const KernelConfig* c = cfgs[i];
         if (force_cfg && std::strcmp(force_cfg, c->name) != 0) continue;
-        for (int split : {1, 2, 4}) {
-            if (fsplit && split != fsplit) continue;
-            if (split > 1 && (ngroups < split || c->bn % 32 != 0)) continue;
-            if (c->smem_bytes(extra_ints, split) > static_cast<size_t>(st.max_smem)) continue;
-            const int cap = split == 1 ? sms : std::min(cluster_capacity(st, i, c, split, extra_ints), sms / split);
-            if (cap <= 0) continue;
-            const long long tiles = static_cast<long long>(m_blocks_total) * ((N + c->bn - 1) / c->bn);
-            const long long waves = (tiles + cap - 1) / cap;
-            const double kb_per = 4.0 * ((ngroups + split - 1) / split);
-            const double t_tile = kb_per * (600.0 + 1.2 * c->bn) + 3000.0 + (split > 1 ? 1500.0 : 0.0);
-            const double cost = static_cast<double>(waves) * t_tile;
-            if (!best.cfg || cost < best_cost - 1e-9) {
-                best.cfg = c;
-                best.split = split;
-                best.capacity = cap;
-                best_cost = cost;
+        for (int pair = 0; pair <= 1; ++pair) {
+            // Pair multicast measured no faster on GB300 (each SM still ingests the whole B
+            // tile), so it is used only when forced.
+            if (fpair >= 0 ? pair != fpair : pair != 0) continue;
+            for (int split : {1, 2, 4}) {
+                if (fsplit && split != fsplit) continue;
+                if (pair && split > 1) continue;
+                if (c->mh > 1 && (split > 1 || pair)) continue;
+                if (split > 1 && (ngroups < split || c->bn % 32 != 0)) continue;
+                if (c->smem_bytes(extra_ints, split) > static_cast<size_t>(st.max_smem)) continue;
+                int cap = sms;
+                if (split > 1)
+                    cap = std::min(cluster_capacity(st, i, c, split, split == 2 ? 0 : 1, split, extra_ints), sms / split);
+                else if (pair)
+                    cap = std::min(cluster_capacity(st, i, c, 2, 3, 1, extra_ints), sms / 2);
+                if (cap <= 0) continue;
+                const long long m_units = (pair || c->mh == 2) ? (m_blocks_total + 1) / 2 : m_blocks_total;
+                const long long tiles = m_units * ((N + c->bn - 1) / c->bn);
+                const long long waves = (tiles + cap - 1) / cap;
+                const double kb_per = 4.0 * ((ngroups + split - 1) / split);
+                const double tma = 2.2 * (128.0 * c->mh + (pair ? c->bn / 2 : c->bn));
+                // one issuer: max(161, N/2 + 33) per MMA; two issuers (MH = 2) keep the pipe at N/2 + 33
+                const double mma = c->mh == 2 ? 8.0 * (c->bn / 2.0 + 33.0) : 4.0 * std::max(161.0, c->bn / 2.0 + 33.0);
+                const double t_tile = kb_per * (std::max(tma, mma) + 20.0) + 3000.0 + (split > 1 ? 1500.0 : 0.0);
+                const double cost = static_cast<double>(waves) * t_tile;
+                if (!best.cfg || cost < best_cost - 1e-9) {
+                    best.cfg = c;
+                    best.split = split;
+                    best.pair = pair;
+                    best.capacity = cap;
+                    best_cost = cost;
+                }
             }
         }
     }
-    (void)mode;
     return best;
 }
 
@@ -247,17 +267,17 @@ dg_status run_gemm(int mode, const void* a, const int32_t* sfa, const void* b, c
     const int m_blocks = (rows + 127) / 128;
     const int Kb = K / 128, Kp = (Kb + 3) / 4;
     const int extra_ints = mode == MODE_MASKED ? groups + 1 : 0;
-    const Plan plan = choose_plan(*st, mode, m_blocks * groups, N, Kb, sms, extra_ints);
+    const Plan plan = choose_plan(*st, m_blocks * groups, N, Kb, sms, extra_ints);
     if (!plan.cfg) return DG_ERR_SHAPE;   // nothing fits in shared memory (too many masked groups)
     const KernelConfig* cfg = plan.cfg;
 
     CUtensorMap maps[4];
     const int a_groups = mode == MODE_MASKED ? groups : 1;
-    if (!encode_3d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, K, rows, a_groups, 128, 128,
+    if (!encode_3d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, K, rows, a_groups, 128, 128 * cfg->mh,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_3d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, K, N, b_groups, 128, cfg->bn,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_3d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfa, al4(rows), Kp, a_groups, 128, 1,
+        !encode_3d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, K, N, b_groups, 128,
+                   plan.pair ? cfg->bn / 2 : cfg->bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_3d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfa, al4(rows), Kp, a_groups, 128 * cfg->mh, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_3d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfb, al4(N), Kp, b_groups, cfg->bn, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -278,23 +298,27 @@ dg_status run_gemm(int mode, const void* a, const int32_t* sfa, const void* b, c
     args.d = static_cast<uint16_t*>(d);
     args.err = st->err_ptr;
     args.timeout_ns = kTimeoutNs;
-    long long units_upper = static_cast<long long>(m_blocks) * groups * args.num_n_blocks;
+    args.pair = plan.pair;
+    args.num_m_units = (plan.pair || cfg->mh == 2) ? (m_blocks + 1) / 2 : m_blocks;
+    long long units_upper = static_cast<long long>(args.num_m_units) * groups * args.num_n_blocks;
+    // 256-row tiles of the contiguous layout get two passes (one per expert when they straddle).
+    const long long passes = (cfg->mh == 2 && mode == MODE_CONTIGUOUS) ? 2 : 1;
     if (mode == MODE_CONTIGUOUS) {
         args.raster_n = args.num_n_blocks;
     } else {
-        args.raster_n = m_blocks >= 16 ? (args.num_n_blocks < 8 ? args.num_n_blocks : 8) : args.num_n_blocks;
+        args.raster_n = args.num_m_units >= 16 ? (args.num_n_blocks < 8 ? args.num_n_blocks : 8) : args.num_n_blocks;
     }
-    args.num_units = mode == MODE_MASKED ? 0 : static_cast<int>(units_upper);
+    args.num_units = mode == MODE_MASKED ? 0 : static_cast<int>(units_upper * passes);
     args.split = plan.split;
-    // Persistent grid: one CTA (or one cluster of `split` CTAs) per co-resident slot.
+    // Persistent grid: one CTA (or one cluster) per co-resident slot.
     const long long slots = units_upper < plan.capacity ? units_upper : plan.capacity;
-    const int grid = static_cast<int>(slots) * plan.split;
+    const int grid = static_cast<int>(slots) * (plan.split > 1 ? plan.split : (plan.pair ? 2 : 1));
     if (env_flag("DG_PRINT_CONFIGS"))
         std::fprintf(stderr,
-                     "[dg] mode=%d groups=%d rows=%d N=%d K=%d -> %s (BN=%d stages=%d acc=%d) split=%d grid=%d "
-                     "raster_n=%d\n",
-                     mode, groups, rows, N, K, cfg->name, cfg->bn, cfg->stages, cfg->acc, plan.split, grid,
-                     args.raster_n);
+                     "[dg] mode=%d groups=%d rows=%d N=%d K=%d -> %s (BN=%d stages=%d acc=%d mh=%d) split=%d pair=%d "
+                     "grid=%d raster_n=%d\n",
+                     mode, groups, rows, N, K, cfg->name, cfg->bn, cfg->stages, cfg->acc, cfg->mh, plan.split,
+                     plan.pair, grid, args.raster_n);
     if (grid <= 0) return DG_OK;
     const cudaError_t e = cfg->launch(maps, args, grid, cs);
     return e == cudaSuccess ? DG_OK : cuda_fail("kernel launch", e);

@@ -3,5 +3,5 @@
 #include "dg_gemm_kernel.cuh"
 
 namespace dg {
-DG_DEFINE_CONFIG(config_bn128_s6_a2, 128, 6, 2)
+DG_DEFINE_CONFIG(config_bn128_s6_a2, 128, 6, 2, 1)
 }  // namespace dg

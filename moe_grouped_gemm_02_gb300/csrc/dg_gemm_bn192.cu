@@ -3,5 +3,5 @@
 #include "dg_gemm_kernel.cuh"
 
 namespace dg {
-DG_DEFINE_CONFIG(config_bn192_s5_a2, 192, 5, 2)
+DG_DEFINE_CONFIG(config_bn192_s5_a2, 192, 5, 2, 1)
 }  // namespace dg

@@ -3,5 +3,5 @@
 #include "dg_gemm_kernel.cuh"
 
 namespace dg {
-DG_DEFINE_CONFIG(config_bn224_s4_a2, 224, 4, 2)
+DG_DEFINE_CONFIG(config_bn224_s4_a2, 224, 4, 2, 1)
 }  // namespace dg

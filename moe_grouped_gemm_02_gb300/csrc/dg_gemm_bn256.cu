@@ -3,5 +3,5 @@
 #include "dg_gemm_kernel.cuh"
 
 namespace dg {
-DG_DEFINE_CONFIG(config_bn256_s4_a1, 256, 4, 1)
+DG_DEFINE_CONFIG(config_bn256_s4_a1, 256, 4, 1, 1)
 }  // namespace dg

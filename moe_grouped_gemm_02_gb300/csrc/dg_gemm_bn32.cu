@@ -3,5 +3,5 @@
 #include "dg_gemm_kernel.cuh"
 
 namespace dg {
-DG_DEFINE_CONFIG(config_bn32_s8_a2, 32, 8, 2)
+DG_DEFINE_CONFIG(config_bn32_s8_a2, 32, 8, 2, 1)
 }  // namespace dg

@@ -8,19 +8,25 @@
 // partial sums to CUDA-core registers to apply the scales; here the tcgen05 block-scaled MMA
 // applies the UE8M0 scales in hardware and accumulates in TMEM, so there is no promotion.
 //
-// One CTA of 6 warps per SM, persistent over output tiles of 128 x BN:
-//   warp 0      TMA producer: A tile [128 x 128], B tile [BN x 128] (128-byte swizzle) and
-//               the packed scale words of both into an S-stage shared-memory ring.
-//   warp 1      allocates TMEM; re-lays the scale words for tcgen05.cp, copies them into
-//               TMEM, and one lane issues four kind::mxf8f6f4 MMAs (K = 32 each) per stage.
-//   warps 2-5   epilogue: TMEM -> registers -> BF16 -> global, one output row per thread.
-// The accumulator is double-buffered in TMEM when it fits (ACC = 2), so the epilogue of
-// one tile overlaps the main loop of the next.
+// One CTA per SM, persistent over output tiles of (128 * MH) x BN, warp-specialised:
+//   warp 0        TMA producer: A tile [128*MH x 128], B tile [BN x 128] (128-byte swizzle)
+//                 into an S-stage ring; the packed scale words of every group of four K
+//                 blocks into a separate 3-slot scale ring.
+//   warp 1 (+7)   MMA issuers, one lane each: kind::mxf8f6f4 block-scaled MMAs (K = 32) into
+//                 TMEM; with MH = 2 each issuer owns one 128-row half of the tile, so two
+//                 instruction streams keep the tensor pipe fed.  Warp 1 also owns TMEM.
+//   warps 2-5     epilogue: TMEM -> registers -> BF16 -> global, one output row per thread
+//   (+8-11)       (with MH = 2 a second set of four writes the second 128-row half).
+//   warp 6        re-lays scale words for tcgen05.cp.
+// With MH = 1 the accumulator can be double-buffered in TMEM (ACC = 2) so that the epilogue
+// of one tile overlaps the main loop of the next.  MH = 2 halves the operand bytes each SM
+// ingests per multiply-add (one B tile serves 256 rows), the limit for large GEMMs.
 //
 // Modes (runtime): dense; M-grouped contiguous (each 128-row block takes the expert of its
 // first row from m_indices, padding rows are written as +0.0); M-grouped masked (the
 // per-group valid-row counts are read on the device, only valid rows are computed and
-// written).
+// written).  Options (runtime, MH = 1): split-K over a cluster of 2 or 4 CTAs reduced through
+// distributed shared memory; CTA pairs sharing B tiles by TMA multicast.
 //
 // Every barrier wait is bounded (GemmArgs::timeout_ns).  On timeout the kernel records the
 // site in the device error word, raises a CTA-wide abort flag, lets every role leave its
@@ -32,33 +38,40 @@
 
 namespace dg {
 
-constexpr int BM = 128;       // rows per tile: the tcgen05 M
+constexpr int BM = 128;       // rows per MMA: the tcgen05 M
 constexpr int BK = 128;       // K per stage: one 128-byte swizzle row, one scale block
 constexpr int MMA_K = 32;     // K of one kind::mxf8f6f4 MMA
-constexpr int NUM_THREADS = 224;
-constexpr uint32_t SF_WARP = 6;     // warp that re-lays scale words for tcgen05.cp
+constexpr uint32_t SF_WARP = 6;      // warp that re-lays scale words for tcgen05.cp
+constexpr uint32_t MMA1_WARP = 7;    // second MMA issuer (MH = 2)
 constexpr int DG_ERR_TIMEOUT_CODE = 6;
 
-template <int BN_, int STAGES_, int ACC_>
+template <int BN_, int STAGES_, int ACC_, int MH_ = 1>
 struct GemmCfg {
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
     static constexpr int ACC = ACC_;
+    static constexpr int MH = MH_;                      // 128-row halves of a tile
+    static constexpr int TM = BM * MH;                  // rows of a tile
+    // warps: producer, MMA issuer, 4 epilogue, scale re-layout (MH = 1); plus a second issuer
+    // and 4 more epilogue warps, one set per 128-row half (MH = 2)
+    static constexpr int THREADS = MH == 2 ? 384 : 224;
+    static constexpr int EPI_THREADS = 128 * MH;
+    static_assert(MH == 1 || MH == 2, "a tile has one or two 128-row halves");
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 16 in [32, 256]");
-    static_assert(ACC == 1 || BN % 32 == 0, "a second accumulator must start on a 32-column boundary");
+    static_assert(BN % 32 == 0 || (ACC == 1 && MH == 1), "accumulators must start on 32-column boundaries");
     static constexpr int SFB_CHUNKS = (BN + 127) / 128;   // 128-row scale chunks of a B tile
-    static constexpr int A_BYTES = BM * BK;
+    static constexpr int A_BYTES = TM * BK;
     static constexpr int B_BYTES = BN * BK;
-    static constexpr int SFA_BYTES = 512;
+    static constexpr int SFA_BYTES = MH * 512;
     static constexpr int SFB_BYTES = SFB_CHUNKS * 512;
     static constexpr uint32_t TX_AB = A_BYTES + B_BYTES;
-    static constexpr uint32_t TX_SF = BM * 4 + BN * 4;
+    static constexpr uint32_t TX_SF = TM * 4 + BN * 4;
     // The packed scale words of a group of four K blocks travel in their own ring of SF_SLOTS
-    // slots (shared memory, then TMEM): TMEM columns are ACC accumulators of BN columns, then
-    // per slot 4 columns of A scales and 4 per 128-row chunk of B scales.
+    // slots (shared memory, then TMEM).  TMEM columns: ACC x MH accumulators of BN columns,
+    // then per slot and per issuer 4 columns of A scales and 4 per 128-row chunk of B scales.
     static constexpr int SF_COLS = 4 + 4 * SFB_CHUNKS;
-    static constexpr int SF_SLOTS = 3;
-    static constexpr int TMEM_USED = ACC * BN + SF_SLOTS * SF_COLS;
+    static constexpr int SF_SLOTS = MH == 2 ? 2 : 3;
+    static constexpr int TMEM_USED = ACC * MH * BN + SF_SLOTS * MH * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64
                                    : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
@@ -72,7 +85,7 @@ struct GemmCfg {
     // slot; split-K reduce: 4 full, 1 empty.
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 3 * SF_SLOTS + 5;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
-    static constexpr int OFF_CUM = OFF_MISC + 16;             // masked mode: m-block prefix sums
+    static constexpr int OFF_CUM = OFF_MISC + 16;             // masked mode: m-unit prefix sums
     // Split-K receive buffer: for every quadrant of rows this CTA owns (4 / split of them), one
     // slot per other CTA of the cluster, 32 rows of BN FP32 (rows padded by 16 bytes).
     static constexpr int RECV_ROW = BN * 4 + 16;
@@ -88,15 +101,37 @@ struct GemmCfg {
 };
 
 struct Unit {
-    int g;      // group of A and D
-    int gb;     // group of B
-    int mb;     // m-block within the group
-    int nb;     // n-block
-    bool zero;  // contiguous mode: the block is padding, write zeros only
+    int g;          // group of A and D
+    int gb;         // group of B
+    int mb;         // m-tile within the group (tile rows mb*128*MH .. +128*MH)
+    int nb;         // n-block
+    bool zero;      // nothing to compute (padding or an empty pass): write zeros / skip
+    bool mc;        // pair mode: the two CTAs of the pair share B, loaded by multicast
+    uint32_t hmask; // MH = 2: the 128-row halves computed in this unit
 };
 
-__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cum, int u) {
+// Unit u of the schedule.
+//  * Plain: m-tile x n-block, in raster bands of raster_n n-blocks (dense, contiguous), or
+//    per group over the device-side prefix sums (masked).
+//  * Pair mode (MH = 1): a unit is an m-block pair; CTA `crank` takes m-block 2*pair+crank.
+//    Both CTAs run the main loop unless both blocks are padding, and share B by multicast
+//    unless the blocks belong to different experts.
+//  * MH = 2, contiguous: each m-tile has two passes; the units of pass 1 follow all those of
+//    pass 0.  If a tile's two halves belong to one expert, pass 0 computes both and pass 1 is
+//    empty; if they belong to two experts, pass h computes half h with that half's expert.
+template <int MH>
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cum, int u, uint32_t crank) {
     Unit t;
+    t.mc = a.pair != 0;
+    t.hmask = MH == 2 ? 3u : 1u;
+    int pass = 0;
+    if (MH == 2 && a.mode == MODE_CONTIGUOUS) {
+        const int per_pass = a.num_units >> 1;
+        if (u >= per_pass) {
+            pass = 1;
+            u -= per_pass;
+        }
+    }
     if (a.mode == MODE_MASKED) {
         // largest g with cum[g] * num_n_blocks <= u; groups with no valid rows are skipped
         int lo = 0, hi = a.groups - 1;
@@ -108,11 +143,12 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cum, i
         const int mbs = cum[lo + 1] - cum[lo];
         t.g = lo;
         t.gb = lo;
-        t.mb = local % mbs;      // m-blocks of one B tile run side by side
+        t.mb = local % mbs;      // m-units of one B tile run side by side
         t.nb = local / mbs;
         t.zero = false;
+        if (a.pair) t.mb = 2 * t.mb + static_cast<int>(crank);
     } else {
-        const int per_band = a.num_m_blocks * a.raster_n;
+        const int per_band = a.num_m_units * a.raster_n;
         const int band = u / per_band;
         const int r = u - band * per_band;
         const int n0 = band * a.raster_n;
@@ -123,9 +159,41 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cum, i
         t.gb = 0;
         t.zero = false;
         if (a.mode == MODE_CONTIGUOUS) {
-            const int e = __ldg(a.m_indices + static_cast<size_t>(t.mb) * BM);
-            t.zero = (e < 0 || e >= a.b_groups);
-            t.gb = t.zero ? 0 : e;
+            auto expert = [&](int blk) {   // expert of 128-row block blk, -1 when none
+                if (blk >= a.num_m_blocks) return -1;
+                const int e = __ldg(a.m_indices + static_cast<size_t>(blk) * BM);
+                return (e >= 0 && e < a.b_groups) ? e : -1;
+            };
+            if (MH == 2) {
+                const int e0 = expert(2 * t.mb), e1 = expert(2 * t.mb + 1);
+                if (e0 < 0 && e1 < 0) {
+                    t.zero = pass == 0;            // all padding: pass 0 writes zeros
+                    t.hmask = pass == 0 ? 3u : 0u;
+                    if (pass) t.zero = true;
+                } else if (e0 < 0 || e1 < 0 || e0 == e1) {
+                    t.gb = e0 >= 0 ? e0 : e1;
+                    t.hmask = pass == 0 ? 3u : 0u;
+                    t.zero = pass != 0;            // one expert: pass 1 is empty
+                } else {
+                    t.gb = pass == 0 ? e0 : e1;    // two experts: one half per pass
+                    t.hmask = 1u << pass;
+                }
+            } else if (a.pair) {
+                const int mu = t.mb;
+                t.mb = 2 * mu + static_cast<int>(crank);
+                const int e_own = expert(t.mb), e_peer = expert(2 * mu + 1 - static_cast<int>(crank));
+                t.zero = e_own < 0 && e_peer < 0;
+                const int gb_own = e_own >= 0 ? e_own : e_peer;
+                const int gb_peer = e_peer >= 0 ? e_peer : e_own;
+                t.gb = t.zero ? 0 : gb_own;
+                t.mc = gb_own == gb_peer;
+            } else {
+                const int e = expert(t.mb);
+                t.zero = e < 0;
+                t.gb = t.zero ? 0 : e;
+            }
+        } else if (a.pair) {
+            t.mb = 2 * t.mb + static_cast<int>(crank);
         }
     }
     return t;
@@ -134,7 +202,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cum, i
 // Bounded wait: true when the phase completed; false after the CTA aborted or this wait
 // timed out (then the error word and abort flag are set).
 static __device__ __noinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                           int* err, unsigned long long timeout_ns, int site) {
+                                                  int* err, unsigned long long timeout_ns, int site) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
@@ -152,7 +220,7 @@ static __device__ __noinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 
 // Same, acquiring at cluster scope: for barriers completed by other CTAs of the cluster.
 static __device__ __noinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                                   int* err, unsigned long long timeout_ns, int site) {
+                                                          int* err, unsigned long long timeout_ns, int site) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
@@ -194,10 +262,11 @@ __device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
 }
 
 template <class C>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(C::THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                     const GemmArgs args) {
+    constexpr int MH = C::MH;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -217,20 +286,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto sffull_bar = [&](int j) { return base + C::OFF_BAR + 8u * (SFB0 + 2 * C::SF_SLOTS + j); };
     auto redfull_bar = [&](int j) { return base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + j); };
     const uint32_t redempty_bar = base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + 4);
-    const int split = args.split;
+    const int split = MH == 1 ? args.split : 1;
+    const int pair = MH == 1 ? args.pair : 0;
     const uint32_t recv_base = base + C::off_recv(args.mode == MODE_MASKED ? args.groups + 1 : 0);
 
     if (threadIdx.x == 0) {
+        // Arrivals per phase: a stage is released by every MMA issuer (and, in pair mode, by
+        // both CTAs of the pair); an accumulator is full once every issuer committed.
+        const uint32_t issuers = MH;
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), pair ? 2u : issuers);
         }
         for (int a = 0; a < C::ACC; ++a) {
-            mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4 * 32);
+            mbar_init(tfull_bar(a), issuers);
+            mbar_init(tempty_bar(a), C::EPI_THREADS);
         }
         for (int j = 0; j < C::SF_SLOTS; ++j) {
-            mbar_init(sfempty_bar(j), 1);
+            mbar_init(sfempty_bar(j), issuers);
             mbar_init(sfready_bar(j), 1);
             mbar_init(sffull_bar(j), 1);
         }
@@ -246,16 +319,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tm_sfb);
     }
     if (args.mode == MODE_MASKED && warp == 2) {
-        // cum[g] = sum over g' < g of ceil(clamp(masked_m[g'], 0, rows) / 128): each lane sums
-        // a contiguous run of groups, then an exclusive warp scan over the runs.
+        // cum[g] = sum over g' < g of the m-units of group g' (128*MH-row tiles, or pairs of
+        // 128-row blocks): each lane sums a contiguous run of groups, then an exclusive warp
+        // scan over the runs.
         const int G = args.groups;
         const int per = (G + 31) / 32;
         const int g0 = min(G, static_cast<int>(lane) * per), g1 = min(G, g0 + per);
-        int run = 0;
-        for (int g = g0; g < g1; ++g) {
+        auto units_of = [&](int g) {
             const int m = min(max(__ldg(args.masked_m + g), 0), args.rows);
-            run += (m + BM - 1) / BM;
-        }
+            const int blocks = (m + C::TM - 1) / C::TM;
+            return pair ? (blocks + 1) / 2 : blocks;
+        };
+        int run = 0;
+        for (int g = g0; g < g1; ++g) run += units_of(g);
         int incl = run;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -265,8 +341,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int acc = incl - run;
         for (int g = g0; g < g1; ++g) {
             cum[g] = acc;
-            const int m = min(max(__ldg(args.masked_m + g), 0), args.rows);
-            acc += (m + BM - 1) / BM;
+            acc += units_of(g);
         }
         if (lane == 31) cum[G] = incl;
     }
@@ -275,20 +350,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before_sync();
-    if (split > 1) cluster_sync_all();   // peers' barriers are initialised before any remote use
+    const bool clustered = split > 1 || pair;
+    if (clustered) cluster_sync_all();   // peers' barriers are initialised before any remote use
     else __syncthreads();
     tc_fence_after_sync();
 
     const uint32_t tmem_base = misc[0];
     // Split-K: the CTAs of a cluster take the same tiles; CTA `crank` covers K-block groups
     // [crank * ngroups / split, (crank + 1) * ngroups / split) (groups of four K blocks).
-    const uint32_t crank = split > 1 ? cluster_ctarank() : 0u;
-    const int u_first = split > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
-    const int u_step = split > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
-    const int ngroups = (args.kblocks + 3) / 4;
-    const int kb0 = 4 * (static_cast<int>(crank) * ngroups / split);
-    const int kb1 = min(args.kblocks, 4 * ((static_cast<int>(crank) + 1) * ngroups / split));
+    const uint32_t crank = clustered ? cluster_ctarank() : 0u;
+    const int u_first = clustered ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int u_step = clustered ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
     const int total_units = args.mode == MODE_MASKED ? cum[args.groups] * args.num_n_blocks : args.num_units;
+    const int ngroups = (args.kblocks + 3) / 4;
+    const int krank = split > 1 ? static_cast<int>(crank) : 0;
+    const int kb0 = 4 * (krank * ngroups / split);
+    const int kb1 = min(args.kblocks, 4 * ((krank + 1) * ngroups / split));
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
@@ -302,7 +379,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t sf_last_par = 0;
             bool ok = true;
             for (int u = u_first; ok && u < total_units; u += u_step) {
-                const Unit t = decode_unit(args, cum, u);
+                const Unit t = decode_unit<MH>(args, cum, u, crank);
                 if (t.zero) continue;
                 const int ga = args.mode == MODE_MASKED ? t.g : 0;
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -318,7 +395,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         sf_phbits ^= 1u << sf_slot;
                         const uint32_t sb = sffull_bar(sf_slot);
                         mbar_arrive_expect_tx(sb, C::TX_SF);
-                        tma_load_3d(base + C::OFF_SFA + sf_slot * C::SFA_BYTES, &tm_sfa, sb, t.mb * BM, kb >> 2, ga);
+                        tma_load_3d(base + C::OFF_SFA + sf_slot * C::SFA_BYTES, &tm_sfa, sb, t.mb * C::TM, kb >> 2, ga);
                         tma_load_3d(base + C::OFF_SFB + sf_slot * C::SFB_BYTES, &tm_sfb, sb, t.nb * C::BN, kb >> 2,
                                     t.gb);
                         sf_last = sf_slot;
@@ -331,8 +408,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const uint32_t fb = full_bar(s);
                     mbar_arrive_expect_tx(fb, C::TX_AB);
-                    tma_load_3d(base + C::OFF_A + s * C::A_BYTES, &tm_a, fb, kb * BK, t.mb * BM, ga);
-                    tma_load_3d(base + C::OFF_B + s * C::B_BYTES, &tm_b, fb, kb * BK, t.nb * C::BN, t.gb);
+                    tma_load_3d(base + C::OFF_A + s * C::A_BYTES, &tm_a, fb, kb * BK, t.mb * C::TM, ga);
+                    if (!pair) {
+                        tma_load_3d(base + C::OFF_B + s * C::B_BYTES, &tm_b, fb, kb * BK, t.nb * C::BN, t.gb);
+                    } else {
+                        // The B map's box is half a tile; with multicast each CTA of the pair loads
+                        // one half into both CTAs, otherwise each loads both halves itself.
+                        constexpr int H = C::BN / 2;
+                        const uint32_t dst = base + C::OFF_B + s * C::B_BYTES;
+                        if (t.mc) {
+                            tma_load_3d_multicast(dst + crank * (H * BK), &tm_b, fb, kb * BK,
+                                                  t.nb * C::BN + static_cast<int>(crank) * H, t.gb, 0x3);
+                        } else {
+                            tma_load_3d(dst, &tm_b, fb, kb * BK, t.nb * C::BN, t.gb);
+                            tma_load_3d(dst + H * BK, &tm_b, fb, kb * BK, t.nb * C::BN + H, t.gb);
+                        }
+                    }
                     ++issued;
                     if (++s == C::STAGES) { s = 0; ph ^= 1u; }
                 }
@@ -352,11 +443,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        // One lane, a minimal loop: the issuing thread's instruction stream is on the critical
-        // path of the tensor pipe, so everything that can happen elsewhere does.
+    } else if (warp == 1 || (MH == 2 && warp == MMA1_WARP)) {
+        // ------------------------------------------------------------------ MMA issuer(s)
+        // One lane per issuer, a minimal loop: the issuing thread's instruction stream is on
+        // the critical path of the tensor pipe, so everything that can happen elsewhere does.
+        // Issuer h computes the tile's 128-row half h into its own accumulator; a unit whose
+        // half h is inactive still walks every barrier (issuing no MMA) to stay in step.
         if (lane == 0) {
+            const uint32_t h = warp == 1 ? 0u : 1u;
             int s = 0;
             uint32_t ph = 0;
             int acc = 0;
@@ -367,22 +461,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             bool any_commit = false;
             uint32_t last_bar = 0, last_par = 0;
-            const uint64_t adesc0 = smem_desc_kmajor_sw128(base + C::OFF_A);
+            const uint64_t adesc0 = smem_desc_kmajor_sw128(base + C::OFF_A + h * (BM * BK));
             const uint64_t bdesc0 = smem_desc_kmajor_sw128(base + C::OFF_B);
             const uint32_t idesc0 = idesc_mxf8_e4m3(BM, C::BN, 0);
             for (int u = u_first; ok && u < total_units; u += u_step) {
-                const Unit t = decode_unit(args, cum, u);
+                const Unit t = decode_unit<MH>(args, cum, u, crank);
                 if (t.zero) continue;
+                const bool active = (t.hmask >> h) & 1u;
                 if (!wait_fast(tempty_bar(acc), acc_ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_TMEM_EMPTY)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * C::BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((acc * MH + h) * C::BN);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if ((kb & 3) == 0) {
                         // First K block of a group: copy the group's re-laid scale words from its
-                        // ring slot into the matching TMEM slot.  (The slot's previous MMAs are
+                        // ring slot into this issuer's TMEM slot.  (The slot's previous MMAs are
                         // complete: the producer waited for that before loading the slot.)
                         if (!wait_fast(sfready_bar(sf_slot), (sfr_phbits >> sf_slot) & 1u, misc + 1, args.err,
                                        args.timeout_ns, SITE_SF_READY)) {
@@ -391,28 +486,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                         sfr_phbits ^= 1u << sf_slot;
                         tc_fence_after_sync();
-                        sfa_t = tmem_base + static_cast<uint32_t>(C::ACC * C::BN + sf_slot * C::SF_COLS);
+                        sfa_t = tmem_base +
+                                static_cast<uint32_t>(C::ACC * MH * C::BN + (sf_slot * MH + h) * C::SF_COLS);
                         sfb_t = sfa_t + 4u;
-                        tc_cp_32x128b_warpx4(sfa_t, smem_desc_sf_chunk(base + C::OFF_SFA + sf_slot * C::SFA_BYTES));
+                        if (active) {
+                            tc_cp_32x128b_warpx4(sfa_t, smem_desc_sf_chunk(base + C::OFF_SFA + sf_slot * C::SFA_BYTES +
+                                                                           h * 512));
 #pragma unroll
-                        for (int c = 0; c < C::SFB_CHUNKS; ++c)
-                            tc_cp_32x128b_warpx4(sfb_t + 4u * c, smem_desc_sf_chunk(base + C::OFF_SFB +
-                                                                                    sf_slot * C::SFB_BYTES + 512 * c));
+                            for (int c = 0; c < C::SFB_CHUNKS; ++c)
+                                tc_cp_32x128b_warpx4(sfb_t + 4u * c, smem_desc_sf_chunk(base + C::OFF_SFB +
+                                                                                        sf_slot * C::SFB_BYTES + 512 * c));
+                        }
                     }
                     if (!wait_fast(full_bar(s), ph, misc + 1, args.err, args.timeout_ns, SITE_FULL)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint64_t adesc = adesc0 + static_cast<uint64_t>((s * C::A_BYTES) >> 4);
-                    const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((s * C::B_BYTES) >> 4);
-                    const uint32_t sf_id = static_cast<uint32_t>(kb & 3);
-                    const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
+                    if (active) {
+                        const uint64_t adesc = adesc0 + static_cast<uint64_t>((s * C::A_BYTES) >> 4);
+                        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((s * C::B_BYTES) >> 4);
+                        const uint32_t sf_id = static_cast<uint32_t>(kb & 3);
+                        const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
 #pragma unroll
-                    for (int k = 0; k < BK / MMA_K; ++k)
-                        tc_mma_mxf8f6f4(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, sfa_t, sfb_t,
-                                        (kb != kb0 || k != 0) ? 1u : 0u);
-                    tc_commit(empty_bar(s));
+                        for (int k = 0; k < BK / MMA_K; ++k)
+                            tc_mma_mxf8f6f4(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, sfa_t, sfb_t,
+                                            (kb != kb0 || k != 0) ? 1u : 0u);
+                    }
+                    if (pair) tc_commit_multicast(empty_bar(s), 0x3);
+                    else tc_commit(empty_bar(s));
                     if ((kb & 3) == 3 || kb == kb1 - 1) {
                         tc_commit(sfempty_bar(sf_slot));
                         if (++sf_slot == C::SF_SLOTS) sf_slot = 0;
@@ -436,13 +538,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ------------------------------------------------------------------ scale re-layout
         // For every group of four K blocks, in order: wait for its scale words to land in their
         // ring slot, re-lay them for tcgen05.cp, publish them to the async proxy and signal the
-        // MMA issuer.  Every party uses each slot's barriers once per group, in group order, so
+        // MMA issuers.  Every party uses each slot's barriers once per group, in group order, so
         // no wait is ever more than one phase from its barrier.
         int sf_slot = 0;
         uint32_t sff_phbits = 0;
         bool ok = true;
         for (int u = u_first; ok && u < total_units; u += u_step) {
-            const Unit t = decode_unit(args, cum, u);
+            const Unit t = decode_unit<MH>(args, cum, u, crank);
             if (t.zero) continue;
             for (int kb = kb0; kb < kb1; kb += 4) {
                 if (!wait_fast(sffull_bar(sf_slot), (sff_phbits >> sf_slot) & 1u, misc + 1, args.err,
@@ -453,7 +555,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 sff_phbits ^= 1u << sf_slot;
                 uint32_t* sfa_w = reinterpret_cast<uint32_t*>(gbase + C::OFF_SFA + sf_slot * C::SFA_BYTES);
                 uint32_t* sfb_w = reinterpret_cast<uint32_t*>(gbase + C::OFF_SFB + sf_slot * C::SFB_BYTES);
-                relayout_sf_chunk(sfa_w, lane);
+#pragma unroll
+                for (int c = 0; c < MH; ++c) relayout_sf_chunk(sfa_w + 128 * c, lane);
 #pragma unroll
                 for (int c = 0; c < C::SFB_CHUNKS; ++c) relayout_sf_chunk(sfb_w + 128 * c, lane);
                 fence_proxy_async_smem();
@@ -462,32 +565,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (++sf_slot == C::SF_SLOTS) sf_slot = 0;
             }
         }
-    } else {
+    } else if ((warp >= 2 && warp <= 5) || (MH == 2 && warp >= 8)) {
         // ------------------------------------------------------------------ epilogue
+        // Warps 2-5 write half 0 of each tile, warps 8-11 (MH = 2) half 1.
         const uint32_t q = warp & 3u;                 // the TMEM lane quadrant this warp may read
-        const int row_in_tile = static_cast<int>(q * 32 + lane);
+        const int my_half = warp >= 8 ? 1 : 0;
+        const int row_in_half = static_cast<int>(q * 32 + lane);
         const int N = args.N;
         int acc = 0;
         uint32_t acc_ph = 0;
         uint32_t red_ph = 0;   // split-K: parity of this warp's reduce barrier
         for (int u = u_first; u < total_units; u += u_step) {
             if (misc[1]) break;
-            const Unit t = decode_unit(args, cum, u);
-            const int row = t.mb * BM + row_in_tile;
+            const Unit t = decode_unit<MH>(args, cum, u, crank);
+            if (t.zero && t.hmask == 0u) continue;     // an empty pass: nothing to write
             const int n0 = t.nb * C::BN;
-            bool write = row < args.rows;
-            bool zero_row = t.zero;
-            if (args.mode == MODE_CONTIGUOUS && write && !zero_row) {
-                const int e = __ldg(args.m_indices + row);
-                zero_row = (e < 0 || e >= args.b_groups);
-            } else if (args.mode == MODE_MASKED) {
-                const int m = min(max(__ldg(args.masked_m + t.g), 0), args.rows);
-                write = row < m;
-            }
-            uint16_t* drow = args.d + (static_cast<size_t>(t.g) * args.rows + row) * static_cast<size_t>(N);
+            const int m_valid = args.mode == MODE_MASKED ? min(max(__ldg(args.masked_m + t.g), 0), args.rows)
+                                                          : args.rows;
+            // Row of half h of this unit for this thread, whether it is stored, and as zeros.
+            auto row_of = [&](int h) { return t.mb * C::TM + h * BM + row_in_half; };
+            auto row_state = [&](int row, bool& write, bool& zero_row) {
+                write = row < m_valid;
+                zero_row = t.zero;
+                if (args.mode == MODE_CONTIGUOUS && write && !zero_row) {
+                    const int e = __ldg(args.m_indices + row);
+                    zero_row = (e < 0 || e >= args.b_groups);
+                }
+            };
+            auto drow_of = [&](int row) {
+                return args.d + (static_cast<size_t>(t.g) * args.rows + row) * static_cast<size_t>(N);
+            };
             if (split > 1) {
                 // Reduce-scatter of the cluster's partial accumulators: quadrant q of the tile's
                 // rows belongs to CTA q / (4 / split); the others send it their partial rows.
+                const int row = row_of(0);
+                bool write, zero_row;
+                row_state(row, write, zero_row);
+                uint16_t* drow = drow_of(row);
                 const uint32_t qpc = 4u / static_cast<uint32_t>(split);
                 const uint32_t owner = q / qpc;
                 const uint32_t lq = q % qpc;
@@ -577,37 +691,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 continue;
             }
             if (t.zero) {
-                if (write)
-                    for (int c = n0; c < min(N, n0 + C::BN); c += 8) st_global_v4(drow + c, make_uint4(0, 0, 0, 0));
+                // Padding only: zeros for every row of the tile, no accumulator involved.
+                {
+                    const int h = my_half;
+                    const int row = row_of(h);
+                    bool write, zero_row;
+                    row_state(row, write, zero_row);
+                    if (write)
+                        for (int c = n0; c < min(N, n0 + C::BN); c += 8)
+                            st_global_v4(drow_of(row) + c, make_uint4(0, 0, 0, 0));
+                }
                 continue;
             }
             if (!wait_or_abort(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
             tc_fence_after_sync();
-            const uint32_t t_row = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * C::BN);
+            {
+                const int h = my_half;
+                if (!((t.hmask >> h) & 1u)) goto epilogue_release;
+                const int row = row_of(h);
+                bool write, zero_row;
+                row_state(row, write, zero_row);
+                uint16_t* drow = drow_of(row);
+                const uint32_t t_row =
+                    tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>((acc * MH + h) * C::BN);
 #pragma unroll 1
-            for (int c = 0; c < (C::BN + 31) / 32; ++c) {
-                uint32_t r[32];
-                const bool half = (C::BN % 32 != 0) && (c == C::BN / 32);   // 16-column tail chunk
-                if (half) tmem_ld_32x32b_x16(t_row + 32u * c, r);
-                else tmem_ld_32x32b_x32(t_row + 32u * c, r);
-                tmem_wait_ld();
-                if (write) {
-                    const int col = n0 + 32 * c;
+                for (int c = 0; c < (C::BN + 31) / 32; ++c) {
+                    uint32_t r[32];
+                    const bool half_chunk = (C::BN % 32 != 0) && (c == C::BN / 32);   // 16-column tail
+                    if (half_chunk) tmem_ld_32x32b_x16(t_row + 32u * c, r);
+                    else tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                    tmem_wait_ld();
+                    if (write) {
+                        const int col = n0 + 32 * c;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (col + 8 * j < N && !(half && j >= 2)) {
-                            uint4 v = make_uint4(0, 0, 0, 0);
-                            if (!zero_row) {
-                                v.x = pack_bf16x2(r[8 * j + 0], r[8 * j + 1]);
-                                v.y = pack_bf16x2(r[8 * j + 2], r[8 * j + 3]);
-                                v.z = pack_bf16x2(r[8 * j + 4], r[8 * j + 5]);
-                                v.w = pack_bf16x2(r[8 * j + 6], r[8 * j + 7]);
+                        for (int j = 0; j < 4; ++j) {
+                            if (col + 8 * j < N && !(half_chunk && j >= 2)) {
+                                uint4 v = make_uint4(0, 0, 0, 0);
+                                if (!zero_row) {
+                                    v.x = pack_bf16x2(r[8 * j + 0], r[8 * j + 1]);
+                                    v.y = pack_bf16x2(r[8 * j + 2], r[8 * j + 3]);
+                                    v.z = pack_bf16x2(r[8 * j + 4], r[8 * j + 5]);
+                                    v.w = pack_bf16x2(r[8 * j + 6], r[8 * j + 7]);
+                                }
+                                st_global_v4(drow + col + 8 * j, v);
                             }
-                            st_global_v4(drow + col + 8 * j, v);
                         }
                     }
                 }
             }
+        epilogue_release:
             tc_fence_before_sync();
             mbar_arrive(tempty_bar(acc));
             if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
@@ -616,7 +748,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     tc_fence_before_sync();
     __syncwarp();
-    if (split > 1) cluster_sync_all();   // no CTA leaves while a peer may still touch its memory
+    if (clustered) cluster_sync_all();   // no CTA leaves while a peer may still touch its memory
     else __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
@@ -628,18 +760,19 @@ template <class C>
 cudaError_t launch_fp8_gemm(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStream_t stream) {
     const int extra = args.mode == MODE_MASKED ? args.groups + 1 : 0;
     const size_t smem = C::smem_bytes(extra, args.split);
-    if (args.split <= 1) {
-        fp8_gemm_kernel<C><<<grid, NUM_THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], args);
+    const int cluster = args.split > 1 ? args.split : (args.pair ? 2 : 1);
+    if (cluster == 1) {
+        fp8_gemm_kernel<C><<<grid, C::THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], args);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(args.split);
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -648,14 +781,14 @@ cudaError_t launch_fp8_gemm(const CUtensorMap* maps, const GemmArgs& args, int g
 }
 
 template <class C>
-int max_clusters_fp8_gemm(int split, size_t smem) {
+int max_clusters_fp8_gemm(int cluster, size_t smem) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(split), 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster), 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -673,10 +806,10 @@ cudaError_t prepare_fp8_gemm(int max_smem) {
     return cudaFuncSetAttribute(fp8_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
 }
 
-#define DG_DEFINE_CONFIG(FN, BN_, ST_, AC_)                                                          \
+#define DG_DEFINE_CONFIG(FN, BN_, ST_, AC_, MH_)                                                     \
     const KernelConfig& FN() {                                                                        \
-        using C = GemmCfg<BN_, ST_, AC_>;                                                             \
-        static const KernelConfig cfg{BN_, ST_, AC_, #FN, &C::smem_bytes, &launch_fp8_gemm<C>,        \
+        using C = GemmCfg<BN_, ST_, AC_, MH_>;                                                        \
+        static const KernelConfig cfg{BN_, ST_, AC_, MH_, #FN, &C::smem_bytes, &launch_fp8_gemm<C>,  \
                                       &prepare_fp8_gemm<C>, &max_clusters_fp8_gemm<C>};               \
         return cfg;                                                                                   \
     }

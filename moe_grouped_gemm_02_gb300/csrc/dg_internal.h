@@ -26,6 +26,8 @@ struct GemmArgs {
     int raster_n;       // n-blocks per raster band (dense and contiguous)
     int num_units;      // tiles to compute (dense and contiguous); masked counts on the device
     int split;          // CTAs (a thread-block cluster) sharing one tile's K range: 1, 2 or 4
+    int pair;           // 1: clusters of 2 CTAs on adjacent m-blocks share each B tile by TMA multicast
+    int num_m_units;    // m-blocks, or m-block pairs when pair == 1 (dense and contiguous)
     const int32_t* m_indices;
     const int32_t* masked_m;
     uint16_t* d;        // BF16 bit patterns
@@ -40,6 +42,7 @@ struct KernelConfig {
     int bn;             // N tile (columns of D per tile)
     int stages;         // shared-memory pipeline depth
     int acc;            // TMEM accumulator buffers
+    int mh;             // 128-row halves per tile (2: one B tile serves 256 rows)
     const char* name;
     size_t (*smem_bytes)(int extra_ints, int split);
     GemmLaunchFn launch;
@@ -55,6 +58,8 @@ const KernelConfig& config_bn128_s6_a2();
 const KernelConfig& config_bn128_s4_a2();
 const KernelConfig& config_bn64_s8_a2();
 const KernelConfig& config_bn32_s8_a2();
+const KernelConfig& config_bn224_s3_m2();
+const KernelConfig& config_bn192_s3_m2();
 
 cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb, int Kb, int Kp,
                            int mn_al, int gran_mn, cudaStream_t stream);
