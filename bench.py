@@ -372,7 +372,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = time_oracle(ws, budget_s=args.cpu_budget, rows_per_workload=160)
+        cpu = time_oracle(ws, budget_s=args.cpu_budget, rows_per_workload=1024)
 
     if rank != 0:
         return None
