@@ -38,6 +38,10 @@
  *    accumulator).
  *  - The environment variable DG_PRINT_CONFIGS=1 prints the kernel configuration chosen
  *    for each call to stderr; DG_NUM_SMS=n caps the SMs used (as dg_set_num_sms).
+ *    DG_FORCE_CONFIG / DG_FORCE_SPLIT / DG_FORCE_PAIR pin the kernel plan (tuning and tests);
+ *    DG_TIMEOUT_MS sets the bound on each in-kernel barrier wait (default 4000) and
+ *    DG_DEBUG_DROP_LOAD=n makes the GEMM skip its n-th load stage, so that a wait runs out:
+ *    a test hook for the timeout path (dg_check_device_error then reports DG_ERR_TIMEOUT).
  */
 #ifndef DG_H
 #define DG_H

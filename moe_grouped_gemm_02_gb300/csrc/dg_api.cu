@@ -297,7 +297,15 @@ dg_status run_gemm(int mode, const void* a, const int32_t* sfa, const void* b, c
     args.masked_m = masked_m;
     args.d = static_cast<uint16_t*>(d);
     args.err = st->err_ptr;
+    // DG_TIMEOUT_MS shortens the bound on every barrier wait and DG_DEBUG_DROP_LOAD=n makes
+    // the producer skip its n-th stage: together they let a test drive the timeout path.
     args.timeout_ns = kTimeoutNs;
+    if (const char* t = std::getenv("DG_TIMEOUT_MS")) {
+        const long long ms = std::atoll(t);
+        if (ms > 0) args.timeout_ns = static_cast<unsigned long long>(ms) * 1000000ull;
+    }
+    args.debug_drop_stage = -1;
+    if (const char* t = std::getenv("DG_DEBUG_DROP_LOAD")) args.debug_drop_stage = std::atoi(t);
     args.pair = plan.pair;
     args.num_m_units = (plan.pair || cfg->mh == 2) ? (m_blocks + 1) / 2 : m_blocks;
     long long units_upper = static_cast<long long>(args.num_m_units) * groups * args.num_n_blocks;

@@ -406,6 +406,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         ok = false;
                         break;
                     }
+                    if (static_cast<int>(issued) == args.debug_drop_stage) {
+                        // Test hook: this stage's barrier is never completed, so its consumer's
+                        // bounded wait runs out and the kernel takes its abort path.
+                        ++issued;
+                        if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+                        continue;
+                    }
                     const uint32_t fb = full_bar(s);
                     mbar_arrive_expect_tx(fb, C::TX_AB);
                     tma_load_3d(base + C::OFF_A + s * C::A_BYTES, &tm_a, fb, kb * BK, t.mb * C::TM, ga);

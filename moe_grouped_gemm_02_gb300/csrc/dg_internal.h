@@ -33,6 +33,7 @@ struct GemmArgs {
     uint16_t* d;        // BF16 bit patterns
     int* err;           // device error word
     unsigned long long timeout_ns;
+    int debug_drop_stage;   // test hook: the producer skips this stage's loads (-1: never)
 };
 
 using GemmLaunchFn = cudaError_t (*)(const CUtensorMap* maps, const GemmArgs& args, int grid,
