@@ -152,6 +152,14 @@ void dg_set_num_sms(int n);
 /* The SM count the next call on the current device will use. */
 int dg_get_num_sms(void);
 
+/* Programmatic dependent launch (README "Utilities": set_pdl).  When enabled (the default;
+ * the environment variable DG_PDL=0 disables it), every kernel of this library is launched so
+ * that its set-up (barrier initialisation, tensor-memory allocation) may overlap the end of the
+ * previous kernel in the stream; each kernel waits for that kernel to complete before it reads
+ * any global memory, so results never depend on the setting.  Process-wide. */
+void dg_set_pdl(int enable);
+int dg_get_pdl(void);
+
 /* A static description of a status code. */
 const char* dg_status_string(dg_status s);
 

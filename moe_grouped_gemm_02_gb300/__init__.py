@@ -26,7 +26,8 @@ _STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_SHAPE", 3: "DG_ERR_AL
 
 EXPORTS = ("dg_fp8_gemm_nt", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_grouped_fp8_gemm_nt_masked",
            "dg_pack_sf_ue8m0", "dg_get_mk_alignment_for_contiguous_layout", "dg_get_tma_aligned_size",
-           "dg_set_num_sms", "dg_get_num_sms", "dg_status_string", "dg_check_device_error")
+           "dg_set_num_sms", "dg_get_num_sms", "dg_set_pdl", "dg_get_pdl", "dg_status_string",
+           "dg_check_device_error")
 
 
 class DGError(RuntimeError):
@@ -63,6 +64,10 @@ def load_library() -> ctypes.CDLL:
     lib.dg_set_num_sms.restype = None
     lib.dg_get_num_sms.argtypes = []
     lib.dg_get_num_sms.restype = i32
+    lib.dg_set_pdl.argtypes = [i32]
+    lib.dg_set_pdl.restype = None
+    lib.dg_get_pdl.argtypes = []
+    lib.dg_get_pdl.restype = i32
     lib.dg_status_string.argtypes = [i32]
     lib.dg_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -105,6 +110,14 @@ def dg_set_num_sms(n: int) -> None:
 
 def dg_get_num_sms() -> int:
     return load_library().dg_get_num_sms()
+
+
+def dg_set_pdl(enable: bool) -> None:
+    load_library().dg_set_pdl(1 if enable else 0)
+
+
+def dg_get_pdl() -> bool:
+    return bool(load_library().dg_get_pdl())
 
 
 def dg_check_device_error(stream=None) -> None:

@@ -30,12 +30,22 @@ struct DeviceState {
     int* err_ptr = nullptr;
     int max_smem = 0;   // opt-in dynamic shared memory per block
     bool prepared = false;
-    int clusters[16][4] = {};   // co-resident clusters per configuration: split 2, split 4, pair (0: unknown)
+    int clusters[16][4] = {};   // co-resident clusters per configuration: split 2, 4, 8, pair (0: unknown)
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 int g_num_sms_cap = -1;   // -1: not read from the environment yet
+int g_pdl = -1;           // programmatic dependent launch: -1 unset (DG_PDL, default on), 0, 1
+
+int pdl_enabled() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_pdl < 0) {
+        const char* v = std::getenv("DG_PDL");
+        g_pdl = (v && v[0] == '0') ? 0 : 1;
+    }
+    return g_pdl;
+}
 
 const KernelConfig* const* all_configs(int* n) {
     static const KernelConfig* cfgs[] = {&config_bn256_s4_a1(), &config_bn224_s4_a2(),
@@ -157,7 +167,8 @@ int cluster_capacity(DeviceState& st, int cfg_index, const KernelConfig* c, int 
     return v;
 }
 
-Plan choose_plan(DeviceState& st, int m_blocks_total, int N, int kblocks, int sms, int extra_ints) {
+Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N, int kblocks, int sms,
+                 int extra_ints) {
     int n = 0;
     const KernelConfig* const* cfgs = all_configs(&n);
     const int ngroups = (kblocks + 3) / 4;
@@ -176,15 +187,20 @@ Plan choose_plan(DeviceState& st, int m_blocks_total, int N, int kblocks, int sm
             // Pair multicast measured no faster on GB300 (each SM still ingests the whole B
             // tile), so it is used only when forced.
             if (fpair >= 0 ? pair != fpair : pair != 0) continue;
-            for (int split : {1, 2, 4}) {
+            for (int split : {1, 2, 4, 8}) {
                 if (fsplit && split != fsplit) continue;
                 if (pair && split > 1) continue;
                 if (c->mh > 1 && (split > 1 || pair)) continue;
+                // Masked groups are filled to an unknown, typically partial, depth: 256-row tiles
+                // would mostly compute padding unless the groups are deep.
+                if (c->mh > 1 && mode == MODE_MASKED && rows < 512 && !force_cfg) continue;
                 if (split > 1 && (ngroups < split || c->bn % 32 != 0)) continue;
                 if (c->smem_bytes(extra_ints, split) > static_cast<size_t>(st.max_smem)) continue;
                 int cap = sms;
                 if (split > 1)
-                    cap = std::min(cluster_capacity(st, i, c, split, split == 2 ? 0 : 1, split, extra_ints), sms / split);
+                    cap = std::min(cluster_capacity(st, i, c, split, split == 2 ? 0 : (split == 4 ? 1 : 2), split,
+                                                    extra_ints),
+                                   sms / split);
                 else if (pair)
                     cap = std::min(cluster_capacity(st, i, c, 2, 3, 1, extra_ints), sms / 2);
                 if (cap <= 0) continue;
@@ -267,7 +283,7 @@ dg_status run_gemm(int mode, const void* a, const int32_t* sfa, const void* b, c
     const int m_blocks = (rows + 127) / 128;
     const int Kb = K / 128, Kp = (Kb + 3) / 4;
     const int extra_ints = mode == MODE_MASKED ? groups + 1 : 0;
-    const Plan plan = choose_plan(*st, m_blocks * groups, N, Kb, sms, extra_ints);
+    const Plan plan = choose_plan(*st, mode, rows, m_blocks * groups, N, Kb, sms, extra_ints);
     if (!plan.cfg) return DG_ERR_SHAPE;   // nothing fits in shared memory (too many masked groups)
     const KernelConfig* cfg = plan.cfg;
 
@@ -305,6 +321,7 @@ dg_status run_gemm(int mode, const void* a, const int32_t* sfa, const void* b, c
         if (ms > 0) args.timeout_ns = static_cast<unsigned long long>(ms) * 1000000ull;
     }
     args.debug_drop_stage = -1;
+    args.pdl = pdl_enabled();
     if (const char* t = std::getenv("DG_DEBUG_DROP_LOAD")) args.debug_drop_stage = std::atoi(t);
     args.pair = plan.pair;
     args.num_m_units = (plan.pair || cfg->mh == 2) ? (m_blocks + 1) / 2 : m_blocks;
@@ -400,7 +417,7 @@ dg_status dg_pack_sf_ue8m0(const float* sf, int32_t* out, int G, int MN, int K, 
     const dg_status s = current_device(&st);
     if (s != DG_OK) return s;
     const int MNb = (MN + gran_mn - 1) / gran_mn;
-    const cudaError_t e = launch_pack_sf(sf, out, G, MN, MNb, Kb, Kp, al4(MN), gran_mn,
+    const cudaError_t e = launch_pack_sf(sf, out, G, MN, MNb, Kb, Kp, al4(MN), gran_mn, pdl_enabled(),
                                          static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
@@ -427,6 +444,13 @@ int dg_get_num_sms(void) {
     }
     return effective_sms(*st);
 }
+
+void dg_set_pdl(int enable) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_pdl = enable ? 1 : 0;
+}
+
+int dg_get_pdl(void) { return pdl_enabled(); }
 
 const char* dg_status_string(dg_status s) {
     switch (s) {

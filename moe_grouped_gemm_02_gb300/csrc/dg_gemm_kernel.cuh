@@ -86,14 +86,14 @@ struct GemmCfg {
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 3 * SF_SLOTS + 5;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
     static constexpr int OFF_CUM = OFF_MISC + 16;             // masked mode: m-unit prefix sums
-    // Split-K receive buffer: for every quadrant of rows this CTA owns (4 / split of them), one
-    // slot per other CTA of the cluster, 32 rows of BN FP32 (rows padded by 16 bytes).
+    // Split-K receive buffer: one slot per other CTA of the cluster, each holding the 128 / split
+    // rows this CTA owns, BN FP32 per row (rows padded by 16 bytes).
     static constexpr int RECV_ROW = BN * 4 + 16;
     static __host__ __device__ uint32_t off_recv(int extra_ints) {
         return (static_cast<uint32_t>(OFF_CUM + extra_ints * 4) + 15u) & ~15u;
     }
     static __host__ __device__ uint32_t recv_bytes(int split) {
-        return split > 1 ? static_cast<uint32_t>((4 / split) * (split - 1) * 32 * RECV_ROW) : 0u;
+        return split > 1 ? static_cast<uint32_t>((split - 1) * (BM / split) * RECV_ROW) : 0u;
     }
     static size_t smem_bytes(int extra_ints, int split) {
         return 1024 + off_recv(extra_ints) + recv_bytes(split);
@@ -308,7 +308,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(sffull_bar(j), 1);
         }
         for (int j = 0; j < 4; ++j) mbar_init(redfull_bar(j), 1);
-        mbar_init(redempty_bar, split > 1 ? 4 - 4 / split : 1);
+        // every other CTA's receiving warps (two when an owner has 64 rows) free the slots once
+        mbar_init(redempty_bar, split > 1 ? static_cast<uint32_t>((split - 1) * (split == 2 ? 2 : 1)) : 1u);
         misc[1] = 0u;
         fence_mbarrier_init();
     }
@@ -318,6 +319,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tma_prefetch_desc(&tm_sfa);
         tma_prefetch_desc(&tm_sfb);
     }
+    if (warp == 1) {
+        tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    // Everything above touches only this CTA's shared and tensor memory, so with programmatic
+    // dependent launch it overlaps the previous kernel; no global memory is read before this.
+    griddep_wait();
+    griddep_launch_dependents();
     if (args.mode == MODE_MASKED && warp == 2) {
         // cum[g] = sum over g' < g of the m-units of group g' (128*MH-row tiles, or pairs of
         // 128-row blocks): each lane sums a contiguous run of groups, then an exclusive warp
@@ -344,10 +353,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             acc += units_of(g);
         }
         if (lane == 31) cum[G] = incl;
-    }
-    if (warp == 1) {
-        tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
-        tmem_relinquish();
     }
     tc_fence_before_sync();
     const bool clustered = split > 1 || pair;
@@ -581,7 +586,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int N = args.N;
         int acc = 0;
         uint32_t acc_ph = 0;
-        uint32_t red_ph = 0;   // split-K: parity of this warp's reduce barrier
+        uint32_t red_eph = 0;  // split-K: parity of the receive-slots-free barrier (sending warps)
+        uint32_t red_fph = 0;  // split-K: parity of this warp's receive barrier (owning warps)
         for (int u = u_first; u < total_units; u += u_step) {
             if (misc[1]) break;
             const Unit t = decode_unit<MH>(args, cum, u, crank);
@@ -603,63 +609,75 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 return args.d + (static_cast<size_t>(t.g) * args.rows + row) * static_cast<size_t>(N);
             };
             if (split > 1) {
-                // Reduce-scatter of the cluster's partial accumulators: quadrant q of the tile's
-                // rows belongs to CTA q / (4 / split); the others send it their partial rows.
+                // Reduce-scatter of the cluster's partial accumulators: rows [o * RPO, (o+1) * RPO)
+                // of the tile belong to CTA o (RPO = 128 / split = 64, 32 or 16 rows).  Every lane
+                // whose row belongs to another CTA sends that CTA its partial row; the owner's
+                // lanes wait for the other split - 1 partials, re-read their own and add.
                 const int row = row_of(0);
                 bool write, zero_row;
                 row_state(row, write, zero_row);
                 uint16_t* drow = drow_of(row);
-                const uint32_t qpc = 4u / static_cast<uint32_t>(split);
-                const uint32_t owner = q / qpc;
-                const uint32_t lq = q % qpc;
+                const uint32_t RPO = BM / static_cast<uint32_t>(split);
+                const uint32_t r_in_tile = q * 32u + lane;
+                const uint32_t owner = r_in_tile / RPO;
+                const bool recv_lane = owner == crank;
+                const uint32_t own0 = crank * RPO, own1 = own0 + RPO;          // rows this CTA owns
+                const bool warp_recv = q * 32u < own1 && q * 32u + 32u > own0;
+                const bool warp_send = !(q * 32u >= own0 && q * 32u + 32u <= own1);
+                // receiving warp index within an owner (RPO = 64: two warps per owner)
+                const uint32_t rw = (r_in_tile % RPO) / 32u;
                 if (t.zero) {
-                    if (owner == crank && write)
+                    if (recv_lane && write)
                         for (int c = n0; c < min(N, n0 + C::BN); c += 8) st_global_v4(drow + c, make_uint4(0, 0, 0, 0));
                     continue;
                 }
                 if (!wait_or_abort(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
                 tc_fence_after_sync();
                 const uint32_t t_row = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * C::BN);
-                if (owner != crank) {
-                    if (!wait_cluster_or_abort(redempty_bar, red_ph ^ 1u, misc + 1, args.err, args.timeout_ns,
+                if (warp_send) {
+                    if (!wait_cluster_or_abort(redempty_bar, red_eph ^ 1u, misc + 1, args.err, args.timeout_ns,
                                                SITE_RED_EMPTY))
                         break;
-                    red_ph ^= 1u;
+                    red_eph ^= 1u;
                     const uint32_t slot = crank < owner ? crank : crank - 1u;
                     const uint32_t dst = map_to_rank(
-                        recv_base + ((lq * (split - 1) + slot) * 32u + lane) * C::RECV_ROW, owner);
-                    const uint32_t rbar = map_to_rank(redfull_bar(static_cast<int>(lq)), owner);
+                        recv_base + (slot * RPO + (r_in_tile - owner * RPO)) * C::RECV_ROW, owner);
+                    const uint32_t rbar = map_to_rank(redfull_bar(static_cast<int>(rw)), owner);
 #pragma unroll 1
                     for (int c = 0; c < C::BN / 32; ++c) {
                         uint32_t r[32];
                         tmem_ld_32x32b_x32(t_row + 32u * c, r);
                         tmem_wait_ld();
+                        if (!recv_lane) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            st_async_v4(dst + 128u * c + 16u * j, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3], rbar);
+                            for (int j = 0; j < 8; ++j)
+                                st_async_v4(dst + 128u * c + 16u * j, r[4 * j], r[4 * j + 1], r[4 * j + 2],
+                                            r[4 * j + 3], rbar);
+                        }
                     }
-                    tc_fence_before_sync();
-                    mbar_arrive(tempty_bar(acc));
-                } else {
-                    if (lane == 0)
-                        mbar_arrive_expect_tx(redfull_bar(static_cast<int>(lq)),
-                                              static_cast<uint32_t>((split - 1) * 32 * C::BN * 4));
-                    if (!wait_cluster_or_abort(redfull_bar(static_cast<int>(lq)), red_ph, misc + 1, args.err,
+                }
+                if (warp_recv) {
+                    if (lane == (own0 > q * 32u ? own0 - q * 32u : 0u))      // first owned lane of the warp
+                        mbar_arrive_expect_tx(redfull_bar(static_cast<int>(rw)),
+                                              static_cast<uint32_t>((split - 1) * min(32u, RPO) * C::BN * 4));
+                    __syncwarp();
+                    if (!wait_cluster_or_abort(redfull_bar(static_cast<int>(rw)), red_fph, misc + 1, args.err,
                                                args.timeout_ns, SITE_RED_FULL))
                         break;
-                    red_ph ^= 1u;
-                    const uint32_t src = recv_base + (lq * (split - 1) * 32u + lane) * C::RECV_ROW;
+                    red_fph ^= 1u;
+                    const uint32_t src = recv_base + (r_in_tile - own0) * C::RECV_ROW;
 #pragma unroll 1
                     for (int c = 0; c < C::BN / 32; ++c) {
                         uint32_t r[32];
                         tmem_ld_32x32b_x32(t_row + 32u * c, r);
                         tmem_wait_ld();
+                        if (!recv_lane) continue;
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
                         for (int sl = 0; sl < split - 1; ++sl) {
                             const float4* p = reinterpret_cast<const float4*>(
-                                gbase + (src - base) + static_cast<uint32_t>(sl) * 32u * C::RECV_ROW + 128u * c);
+                                gbase + (src - base) + static_cast<uint32_t>(sl) * RPO * C::RECV_ROW + 128u * c);
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
                                 const float4 x = p[j];
@@ -686,10 +704,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             }
                         }
                     }
-                    tc_fence_before_sync();
-                    mbar_arrive(tempty_bar(acc));
+                }
+                tc_fence_before_sync();
+                mbar_arrive(tempty_bar(acc));
+                if (warp_recv) {
+                    // The receive slots of this warp's rows may be refilled: tell every other CTA.
                     __syncwarp();
-                    if (lane == 0)
+                    if (lane == (own0 > q * 32u ? own0 - q * 32u : 0u))
                         for (int rk = 0; rk < split; ++rk)
                             if (static_cast<uint32_t>(rk) != crank)
                                 mbar_arrive_remote(map_to_rank(redempty_bar, static_cast<uint32_t>(rk)));
@@ -768,22 +789,27 @@ cudaError_t launch_fp8_gemm(const CUtensorMap* maps, const GemmArgs& args, int g
     const int extra = args.mode == MODE_MASKED ? args.groups + 1 : 0;
     const size_t smem = C::smem_bytes(extra, args.split);
     const int cluster = args.split > 1 ? args.split : (args.pair ? 2 : 1);
-    if (cluster == 1) {
-        fp8_gemm_kernel<C><<<grid, C::THREADS, smem, stream>>>(maps[0], maps[1], maps[2], maps[3], args);
-        return cudaGetLastError();
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (args.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<C>, maps[0], maps[1], maps[2], maps[3], args);
 }
 

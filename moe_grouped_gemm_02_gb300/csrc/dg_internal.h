@@ -34,6 +34,7 @@ struct GemmArgs {
     int* err;           // device error word
     unsigned long long timeout_ns;
     int debug_drop_stage;   // test hook: the producer skips this stage's loads (-1: never)
+    int pdl;                // launch with programmatic dependent launch
 };
 
 using GemmLaunchFn = cudaError_t (*)(const CUtensorMap* maps, const GemmArgs& args, int grid,
@@ -63,6 +64,6 @@ const KernelConfig& config_bn224_s3_m2();
 const KernelConfig& config_bn192_s3_m2();
 
 cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb, int Kb, int Kp,
-                           int mn_al, int gran_mn, cudaStream_t stream);
+                           int mn_al, int gran_mn, int pdl, cudaStream_t stream);
 
 }  // namespace dg

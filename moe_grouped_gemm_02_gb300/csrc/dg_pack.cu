@@ -6,6 +6,7 @@
 // Output word [g][kp][r], byte j = UE8M0 code of the scale of row r and K block 4*kp + j.
 // One thread per output word, rows fastest: the stores of a warp are 128 contiguous bytes.
 #include "dg_internal.h"
+#include "dg_ptx.cuh"
 
 namespace dg {
 
@@ -25,6 +26,8 @@ __device__ __forceinline__ uint32_t ue8m0_code_ceil(float x) {
 
 __global__ void __launch_bounds__(256) pack_sf_kernel(const float* __restrict__ sf, int32_t* __restrict__ out,
                                                       int MN, int MNb, int Kb, int Kp, int mn_al, int gran_mn) {
+    griddep_wait();   // with programmatic dependent launch: the inputs' producer has finished
+    griddep_launch_dependents();
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     const int kp = blockIdx.y;
     const int g = blockIdx.z;
@@ -42,10 +45,17 @@ __global__ void __launch_bounds__(256) pack_sf_kernel(const float* __restrict__ 
 }
 
 cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb, int Kb, int Kp,
-                           int mn_al, int gran_mn, cudaStream_t stream) {
-    const dim3 grid((mn_al + 255) / 256, Kp, G);
-    pack_sf_kernel<<<grid, 256, 0, stream>>>(sf, out, MN, MNb, Kb, Kp, mn_al, gran_mn);
-    return cudaGetLastError();
+                           int mn_al, int gran_mn, int pdl, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((mn_al + 255) / 256, Kp, G);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, pack_sf_kernel, sf, out, MN, MNb, Kb, Kp, mn_al, gran_mn);
 }
 
 }  // namespace dg

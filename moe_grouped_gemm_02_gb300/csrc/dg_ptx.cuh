@@ -76,6 +76,19 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 }
 
 // ---------------------------------------------------------------------------------------
+// Programmatic dependent launch
+// ---------------------------------------------------------------------------------------
+// Blocks until the grids this grid depends on have completed and their memory is visible
+// (returns at once when the grid was launched without a programmatic dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the grid that depends on this one start launching (its blocks still wait, in
+// griddep_wait, for this grid to complete before they read anything it writes).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------------
 // Thread-block clusters and distributed shared memory
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -172,3 +172,25 @@ def test_masked_parity(G, max_m, N, K, masked_m):
     rows = np.arange(max_m)[None, :] < np.asarray(masked_m)[:, None]
     assert np.array_equal(got[~rows], want[~rows]), "rows past masked_m must stay untouched"
     assert_within_tolerance(got[rows], want[rows], f"masked {masked_m}")
+
+
+@pytest.mark.parametrize("pdl", [False, True])
+def test_programmatic_dependent_launch_setting(pdl):
+    # Results must not depend on whether kernels may start before the previous one finished:
+    # a kernel writing the inputs runs right before the GEMM on the same stream.
+    prev = dg.dg_get_pdl()
+    dg.dg_set_pdl(pdl)
+    try:
+        w = synth.make_dense(256, 1024, 1536, seed=41)
+        sfa = oracle.pack_sf_ue8m0(w["sfa"], 256, 1)[0]
+        sfb = oracle.pack_sf_ue8m0(w["sfb"], 1024, 128)[0]
+        a = torch.zeros((256, 1536), dtype=torch.uint8, device="cuda")
+        src = to_dev(w["a"])
+        d = torch.empty((256, 1024), dtype=torch.int16, device="cuda")
+        a.copy_(src)                                   # produces A immediately before the GEMM
+        dg.dg_fp8_gemm_nt(a, to_dev(sfa), to_dev(w["b"]), to_dev(sfb), d)
+        dg.dg_check_device_error()
+        assert dg.dg_get_pdl() == pdl
+        assert_within_tolerance(bits(d), oracle.fp8_gemm_nt(w["a"], sfa, w["b"], sfb), f"pdl={pdl}")
+    finally:
+        dg.dg_set_pdl(prev)

@@ -59,7 +59,7 @@ def test_dense_every_plan(cfg, split, few_sms, monkeypatch):
     assert_within_tolerance(bits(d), want, f"{cfg} split {split}")
 
 
-@pytest.mark.parametrize("split", [2, 4])
+@pytest.mark.parametrize("split", [2, 4, 8])
 def test_split_k_decode_shape(split, monkeypatch):
     monkeypatch.setenv("DG_FORCE_SPLIT", str(split))
     M, N, K = 64, 2112, 7168
@@ -183,3 +183,32 @@ def test_contiguous_256_row_tiles_straddling_experts(cfg, few_sms, monkeypatch):
     assert np.all(got[~valid] == 0)
     want = oracle.m_grouped_fp8_gemm_nt_contiguous(c["a"], csfa, c["b"], csfb, c["m_indices"])
     assert_within_tolerance(got[valid], want[valid], f"contiguous 256-row tiles {cfg}")
+
+
+@pytest.mark.parametrize("cfg", ["config_bn128_s4_a2", "config_bn64_s8_a2", "config_bn32_s8_a2"])
+@pytest.mark.parametrize("split", [2, 4, 8])
+def test_split_k_rows_per_owner(cfg, split, few_sms, monkeypatch):
+    # 128 / split rows of each tile per owning CTA (64, 32, 16); 36 K blocks = 9 groups, so the
+    # 8-way split has uneven K ranges; ragged M and N.
+    monkeypatch.setenv("DG_FORCE_CONFIG", cfg)
+    monkeypatch.setenv("DG_FORCE_SPLIT", str(split))
+    M, N, K = 200, 448, 4608
+    w, sfa, sfb, want = _dense(M, N, K, seed=split * 10 + len(cfg))
+    d = torch.full((M, N), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
+    _call_or_skip(dg.dg_fp8_gemm_nt, to_dev(w["a"]), to_dev(sfa), to_dev(w["b"]), to_dev(sfb), d)
+    dg.dg_check_device_error()
+    assert_within_tolerance(bits(d), want, f"{cfg} split {split}")
+    # masked layout with the same split
+    m = synth.make_masked(2, 160, 192, K, seed=split, masked_m=[160, 17])
+    msfa = oracle.pack_sf_ue8m0(m["sfa"], 160, 1)
+    msfb = oracle.pack_sf_ue8m0(m["sfb"], 192, 128)
+    md = torch.full((2, 160, 192), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
+    dg.dg_m_grouped_fp8_gemm_nt_masked(to_dev(m["a"]), to_dev(msfa), to_dev(m["b"]), to_dev(msfb), md,
+                                      to_dev(m["masked_m"]))
+    dg.dg_check_device_error()
+    prior = np.full((2, 160, 192), synth.SENTINEL_BF16, np.uint16)
+    wantm = oracle.m_grouped_fp8_gemm_nt_masked(m["a"], msfa, m["b"], msfb, m["masked_m"], prior)
+    got = bits(md)
+    rows = np.arange(160)[None, :] < m["masked_m"][:, None]
+    assert np.array_equal(got[~rows], wantm[~rows])
+    assert_within_tolerance(got[rows], wantm[rows], f"masked {cfg} split {split}")
