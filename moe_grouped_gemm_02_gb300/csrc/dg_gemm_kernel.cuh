@@ -356,8 +356,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     tc_fence_before_sync();
     const bool clustered = split > 1 || pair;
-    if (clustered) cluster_sync_all();   // peers' barriers are initialised before any remote use
-    else __syncthreads();
+    // The producer needs nothing another warp prepares (except the masked-mode prefix sums),
+    // and outside pair mode it only writes its own CTA's shared memory: it arrives without
+    // waiting and starts loading at once.  Everyone else waits for the barrier initialisation,
+    // the TMEM address and, in a cluster, for every peer to be initialised.
+    const bool early_producer = warp == 0 && args.mode != MODE_MASKED && !pair;
+    if (clustered) {
+        cluster_arrive();
+        if (!early_producer) cluster_wait();
+    } else if (early_producer) {
+        named_bar_arrive(1, C::THREADS);
+    } else {
+        named_bar_sync(1, C::THREADS);
+    }
     tc_fence_after_sync();
 
     const uint32_t tmem_base = misc[0];
@@ -776,6 +787,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
     tc_fence_before_sync();
     __syncwarp();
+    if (clustered && early_producer) cluster_wait();   // completes the start-up barrier phase
     if (clustered) cluster_sync_all();   // no CTA leaves while a peer may still touch its memory
     else __syncthreads();
     if (warp == 1) {
