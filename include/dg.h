@@ -138,6 +138,25 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
 dg_status dg_pack_sf_ue8m0(const float* sf, int32_t* out, int G, int MN, int K, int gran_mn,
                            int gran_k, void* stream);
 
+/*
+ * Per-token 1x128 FP8 quantisation of BF16 activations, writing the packed scales directly
+ * (README "Interface / Notes": FP8 quantisation of the inputs is left to the caller, to be
+ * implemented separately or fused into the kernel that produces them).
+ *
+ *   x   bf16  [G][M][K]          row-major, finite values (a NaN or Inf gives unspecified codes)
+ *   q   e4m3  [G][M][K]          row-major; fully overwritten
+ *   sf  int32 [G][Kp][al4(M)]    packed UE8M0 scales in the A-operand layout of the GEMMs;
+ *                                fully overwritten, padding rows [M, al4(M)) and bytes of
+ *                                K blocks >= Kb are 0
+ * For each row and 1x128 block: amax = max |x|; e = the smallest integer with
+ * 448 * 2^e >= amax, clamped to [-127, 127], and 0 when amax = 0; the scale byte is e + 127
+ * and the codes are round-to-nearest-even of x * 2^-e (|x * 2^-e| <= 448: no saturation).
+ * G = 1 with M = M_sum quantises a contiguous-layout A; G groups of max_m rows a masked one.
+ * Requires G > 0, M >= 0 (0 is a no-op), K > 0 with K % 128 == 0, 16-byte aligned pointers.
+ * Asynchronous on `stream`; buffers are the caller's; nothing is allocated.
+ */
+dg_status dg_quantize_fp8_1x128(const void* x, void* q, int32_t* sf, int G, int M, int K, void* stream);
+
 /* Row alignment of expert segments in the contiguous layout (the GEMM M block): 128.
  * (README "Grouped GEMM (contiguous layout)": get_mk_alignment_for_contiguous_layout.) */
 int dg_get_mk_alignment_for_contiguous_layout(void);

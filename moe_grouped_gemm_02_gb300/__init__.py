@@ -27,7 +27,7 @@ _STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_SHAPE", 3: "DG_ERR_AL
 EXPORTS = ("dg_fp8_gemm_nt", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_grouped_fp8_gemm_nt_masked",
            "dg_pack_sf_ue8m0", "dg_get_mk_alignment_for_contiguous_layout", "dg_get_tma_aligned_size",
            "dg_set_num_sms", "dg_get_num_sms", "dg_set_pdl", "dg_get_pdl", "dg_status_string",
-           "dg_check_device_error")
+           "dg_check_device_error", "dg_quantize_fp8_1x128")
 
 
 class DGError(RuntimeError):
@@ -52,8 +52,9 @@ def load_library() -> ctypes.CDLL:
     lib.dg_m_grouped_fp8_gemm_nt_contiguous.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     lib.dg_m_grouped_fp8_gemm_nt_masked.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     lib.dg_pack_sf_ue8m0.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp]
+    lib.dg_quantize_fp8_1x128.argtypes = [vp, vp, vp, i32, i32, i32, vp]
     for name in ("dg_fp8_gemm_nt", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_grouped_fp8_gemm_nt_masked",
-                 "dg_pack_sf_ue8m0", "dg_check_device_error"):
+                 "dg_pack_sf_ue8m0", "dg_check_device_error", "dg_quantize_fp8_1x128"):
         getattr(lib, name).restype = i32
     lib.dg_check_device_error.argtypes = [vp]
     lib.dg_get_mk_alignment_for_contiguous_layout.argtypes = []
@@ -156,6 +157,15 @@ def dg_pack_sf_ue8m0(sf, out, mn: int, gran_mn: int, stream=None) -> None:
     Kb = sf.shape[-1]
     _check("dg_pack_sf_ue8m0", load_library().dg_pack_sf_ue8m0(
         _ptr(sf, "sf"), _ptr(out, "out"), G, int(mn), Kb * 128, int(gran_mn), 128, _stream(stream)))
+
+
+def dg_quantize_fp8_1x128(x, q, sf, stream=None) -> None:
+    """Quantises bf16 x [G?][M][K] into e4m3 codes q (same shape, uint8) and packed scales
+    sf int32 [G?][Kp][al4(M)]."""
+    G = x.shape[0] if x.dim() == 3 else 1
+    M, K = x.shape[-2], x.shape[-1]
+    _check("dg_quantize_fp8_1x128", load_library().dg_quantize_fp8_1x128(
+        _ptr(x, "x"), _ptr(q, "q"), _ptr(sf, "sf"), G, M, K, _stream(stream)))
 
 
 def packed_sf_shape(groups: int | None, mn: int, K: int) -> tuple:

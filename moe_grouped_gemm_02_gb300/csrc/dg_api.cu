@@ -422,6 +422,19 @@ dg_status dg_pack_sf_ue8m0(const float* sf, int32_t* out, int G, int MN, int K, 
     return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 
+dg_status dg_quantize_fp8_1x128(const void* x, void* q, int32_t* sf, int G, int M, int K, void* stream) {
+    if (!x || !q || !sf || G <= 0 || M < 0 || K <= 0) return DG_ERR_INVALID_ARG;
+    if (K % 128 != 0) return DG_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return DG_ERR_ALIGNMENT;
+    if (M == 0) return DG_OK;
+    DeviceState* st = nullptr;
+    const dg_status s = current_device(&st);
+    if (s != DG_OK) return s;
+    const cudaError_t e = launch_quantize_fp8_1x128(x, q, sf, G, M, K, pdl_enabled(), static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return DG_ERR_SHAPE;
+    return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
 int dg_get_mk_alignment_for_contiguous_layout(void) { return 128; }
 
 int dg_get_tma_aligned_size(int mn, int elem_bytes) {

@@ -65,5 +65,7 @@ const KernelConfig& config_bn192_s3_m2();
 
 cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb, int Kb, int Kp,
                            int mn_al, int gran_mn, int pdl, cudaStream_t stream);
+cudaError_t launch_quantize_fp8_1x128(const void* x, void* q, int32_t* sf, int G, int M, int K, int pdl,
+                                      cudaStream_t stream);
 
 }  // namespace dg

@@ -35,10 +35,12 @@ Readings where the pages are silent (each listed in the design notes):
   P7  the exact sum is rounded once to BF16, round-to-nearest-even.
   P8  contiguous-layout padding rows (m_indices == -1) come out as +0.0.
   P9  masked-layout rows at or past masked_m[g] keep whatever D held before.
+  P1  (per-token quantisation) the scale of a 1x128 block is 2**e with e the smallest integer
+      such that 448 * 2**e >= amax, clamped to [-127, 127], 0 for an all-zero block.
 """
 from .reference import (  # noqa: F401
     e4m3_decode_table, e4m3_decode, ue8m0_decode, ue8m0_encode, tma_aligned_size,
     pack_sf_ue8m0, unpack_sf_ue8m0, bf16_round_bits, bf16_bits_to_float,
     fp8_gemm_nt, fp8_gemm_nt_unrounded, m_grouped_fp8_gemm_nt_contiguous,
-    m_grouped_fp8_gemm_nt_masked,
+    m_grouped_fp8_gemm_nt_masked, e4m3_encode_rne, block_scale_exponent, quantize_fp8_1x128,
 )

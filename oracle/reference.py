@@ -256,3 +256,62 @@ def _repack_rows(codes_rows: np.ndarray) -> np.ndarray:
         kp, j = divmod(kb, 4)
         out[kp, :R] |= codes_rows[:, kb].astype(np.uint32) << (8 * j)
     return out.view(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# Per-token 1x128 quantisation (README "Interface / Notes": FP8 casting is the caller's job,
+# to be fused into an earlier kernel; this is the operation such a kernel performs)
+# ---------------------------------------------------------------------------
+
+_POS_CODES = np.arange(0x7F)                 # codes 0x00..0x7E: the non-negative finite values
+_POS_VALUES = _E4M3[:0x7F]                   # increasing
+
+
+def e4m3_encode_rne(v: np.ndarray) -> np.ndarray:
+    """float64 values with |v| <= 448 -> E4M3 codes, round to nearest, ties to the even code.
+
+    The nearest of the 127 non-negative finite values is found by search; on a tie the code
+    whose mantissa bit 0 is clear wins.  The sign bit is the sign of v (so -0.0 -> 0x80).
+    """
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    assert np.all(a <= 448.0), "values beyond the E4M3 range"
+    hi = np.searchsorted(_POS_VALUES, a, side="left")          # first value >= a
+    hi = np.minimum(hi, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_hi = _POS_VALUES[hi] - a
+    d_lo = a - _POS_VALUES[lo]
+    exact = d_hi == 0
+    pick_hi = exact | (d_hi < d_lo) | ((d_hi == d_lo) & ((_POS_CODES[hi] & 1) == 0))
+    code = np.where(pick_hi, _POS_CODES[hi], _POS_CODES[lo]).astype(np.uint8)
+    return np.where(np.signbit(v), code | 0x80, code).astype(np.uint8)
+
+
+def block_scale_exponent(amax: np.ndarray) -> np.ndarray:
+    """Smallest integer e with 448 * 2**e >= amax, clamped to [-127, 127]; 0 when amax == 0.
+
+    Found by walking e from the frexp exponent of amax (448 * 2**e is exact in float64).
+    """
+    a = np.asarray(amax, dtype=np.float64)
+    _, fe = np.frexp(a)
+    e = fe.astype(np.int64) - 10                               # 448 * 2**(fe-10) < 2**(fe-1) <= a
+    for _ in range(3):                                         # at most two steps up
+        e = np.where(np.ldexp(448.0, e) < a, e + 1, e)
+    e = np.clip(e, -127, 127)
+    return np.where(a == 0, 0, e).astype(np.int64)
+
+
+def quantize_fp8_1x128(x: np.ndarray):
+    """x [M, K] (any float dtype, finite) -> (E4M3 codes [M, K], packed UE8M0 int32 [Kp][al4(M)]).
+
+    Per 1x128 block of a row: e = block_scale_exponent(amax), codes = RNE(x / 2**e).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    M, K = x.shape
+    assert K % BLOCK_K == 0
+    xb = x.reshape(M, K // BLOCK_K, BLOCK_K)
+    e = block_scale_exponent(np.abs(xb).max(axis=-1))          # [M, Kb]
+    scaled = xb / np.ldexp(1.0, e)[..., None]                  # exact: division by a power of two
+    codes = e4m3_encode_rne(scaled).reshape(M, K)
+    packed = pack_sf_ue8m0(np.ldexp(1.0, e).astype(np.float32), M, 1)[0]
+    return codes, packed

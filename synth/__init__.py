@@ -41,7 +41,7 @@ NAN_CODE = 0x7F      # E4M3 NaN bit pattern, used to poison padding rows
 # Stream ids, one per tensor role, so that changing one tensor's shape does not
 # shift the random numbers of another.
 _STREAM = {"a": 1, "b": 2, "outlier": 3, "counts": 4, "masked_m": 5, "perm": 6,
-           "d_fill": 7, "sf": 8}
+           "d_fill": 7, "sf": 8, "act": 9}
 
 
 def rng(seed: int, role: str, sub: int = 0) -> np.random.Generator:
@@ -195,6 +195,25 @@ SENTINEL_BF16 = 0x7FA5   # a NaN pattern used to pre-fill D where rows must stay
 
 
 # The five workloads, by name.  Sizes from the DeepGEMM article's H800 tables.
+def make_activations(G: int, M: int, K: int, seed: int = 0, wide: bool = False) -> np.ndarray:
+    """BF16 activations [G, M, K] as uint16 bit patterns: N(0,1) with 1% outliers x20.
+
+    wide=True stresses the scale range: every row gets its own magnitude 2**U{-120..110},
+    every fifth 1x128 block is zero, and some rows hold BF16 subnormals and values two
+    hundred binades below their block's maximum.
+    """
+    x = add_outliers(normal((G, M, K), seed, "act"), seed, sub=9)
+    if wide:
+        r = rng(seed, "act", 1)
+        x *= np.ldexp(np.float32(1.0), r.integers(-120, 111, size=(G, M, 1)))
+        xb = x.reshape(G, M, K // BLOCK, BLOCK)
+        xb[:, :, ::5, :] = 0.0
+        if M > 2:
+            x[:, 1, :] = np.ldexp(np.float32(1.0), -130) * r.integers(-7, 8, size=(G, K))   # subnormals
+            x[:, 2, :] = np.ldexp(normal((G, K), seed, "act", sub=2), r.integers(-126, 101, size=(G, K)))
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
 DECODE_SHAPES = [(64, 2112, 7168), (128, 24576, 1536), (128, 7168, 2048), (64, 4096, 7168)]
 PREFILL_SHAPE = (4096, 7168, 16384)
 CONTIGUOUS = dict(G=4, N=4096, K=7168, tokens=32768)

@@ -79,3 +79,12 @@ def test_pack_validation(lib):
     assert f(GOOD, GOOD, 1, 64, 1000, 1, 128, None) == 2
     assert f(GOOD, ODD, 1, 64, 1024, 1, 128, None) == 3
     assert f(GOOD, GOOD, 1, 0, 1024, 1, 128, None) == 0
+
+
+def test_quantize_validation(lib):
+    f = lib.dg_quantize_fp8_1x128
+    assert f(None, GOOD, GOOD, 1, 64, 1024, None) == 1        # null input
+    assert f(GOOD, GOOD, GOOD, 0, 64, 1024, None) == 1        # G == 0
+    assert f(GOOD, GOOD, GOOD, 1, 64, 1000, None) == 2        # K % 128
+    assert f(GOOD, GOOD, ODD, 1, 64, 1024, None) == 3         # misaligned scales
+    assert f(GOOD, GOOD, GOOD, 1, 0, 1024, None) == 0         # empty: no-op

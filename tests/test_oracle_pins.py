@@ -417,3 +417,62 @@ def test_masked_equals_dense_and_keeps_prior_rows():
             dense = oracle.fp8_gemm_nt(a[g, :m], oracle.pack_sf_ue8m0(
                 np.ldexp(1.0, ea[g, :m]).astype(np.float32), int(m), 1)[0], b[g], sfb[g])
             assert np.array_equal(d[g, :m], dense)
+
+
+# ---------------------------------------------------------------------------
+# Per-token quantisation
+# ---------------------------------------------------------------------------
+
+def test_e4m3_encode_matches_torch_cast_on_float32():
+    # torch's float32 -> float8_e4m3fn cast is an independent RNE implementation
+    rs = np.random.default_rng(21)
+    v = (rs.uniform(-448, 448, 20000) * 2.0 ** rs.integers(-14, 1, 20000)).astype(np.float32)
+    mids = (oracle.e4m3_decode_table()[:0x7E] + oracle.e4m3_decode_table()[1:0x7F]) / 2
+    v = np.concatenate([v, mids.astype(np.float32), -mids.astype(np.float32),
+                        np.float32([0.0, -0.0, 448.0, -448.0, 2.0 ** -10, 3 * 2.0 ** -10])])
+    want = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.e4m3_encode_rne(v.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+def test_block_scale_exponent_definition():
+    amax = np.array([448.0, 448.0 * (1 + 2.0 ** -52), 448.0 * 2 ** -3, 1.0, 0.0, 2.0 ** -140, 3.0e38, 224.0, 225.0])
+    e = oracle.block_scale_exponent(amax)
+    for a, ei in zip(amax, e):
+        if a == 0:
+            assert ei == 0
+            continue
+        if -127 < ei < 127:
+            assert 448.0 * 2.0 ** int(ei) >= a and 448.0 * 2.0 ** (int(ei) - 1) < a
+    assert list(e[:4]) == [0, 1, -3, -8] and e[5] == -127 and e[7] == -1 and e[8] == 0
+
+
+def test_quantize_round_trip_and_bounds():
+    rs = np.random.default_rng(22)
+    x = rs.standard_normal((5, 384)) * 10.0 ** rs.integers(-3, 4, (5, 1))
+    x[2, 128:256] = 0.0                                      # an all-zero block
+    codes, packed = oracle.quantize_fp8_1x128(x)
+    e = oracle.unpack_sf_ue8m0(packed, 5, 3)[0].astype(np.int64) - 127
+    deq = oracle.e4m3_decode(codes).reshape(5, 3, 128) * np.ldexp(1.0, e)[..., None]
+    xb = x.reshape(5, 3, 128)
+    err = np.abs(deq - xb)
+    # within half an E4M3 ulp of the scaled value (3 mantissa bits, subnormal below 2**-6)
+    scaled = np.abs(xb) / np.ldexp(1.0, e)[..., None]
+    E = np.floor(np.log2(np.maximum(scaled, 2.0 ** -30)))
+    half_ulp = np.ldexp(1.0, (np.maximum(E, -6) - 4).astype(np.int64)) * np.ldexp(1.0, e)[..., None]
+    assert np.all(err <= half_ulp)
+    assert e[2, 1] == 0 and np.all(codes[2, 128:256] == 0)
+    amax_q = np.abs(oracle.e4m3_decode(codes)).reshape(5, 3, 128).max(-1)
+    assert np.all((amax_q[e != 0] >= 224) & (amax_q[e != 0] <= 448))
+
+
+def test_quantize_agrees_with_the_input_generator_on_bf16_activations():
+    # The input generator quantises with frexp and torch's cast; the oracle with a search over
+    # the E4M3 table and an exponent walk.  On BF16 inputs both must give the same bytes.
+    import synth
+    x = synth.make_activations(1, 6, 1280, seed=4, wide=True)[0]
+    xf = oracle.bf16_bits_to_float(x)
+    codes, packed = oracle.quantize_fp8_1x128(xf)
+    s_codes, s_sf = synth.quantize_1x128(xf.astype(np.float32))
+    assert np.array_equal(codes, s_codes)
+    assert np.array_equal(packed, oracle.pack_sf_ue8m0(s_sf, 6, 1)[0])
