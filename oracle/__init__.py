@@ -24,6 +24,13 @@ float64, so that it can be checked against the pages by eye:
   * the M-grouped contiguous and masked layouts (README "Grouped GEMM
     (contiguous layout)" and "Grouped GEMM (masked layout)"; the article's §五.1
     layout table).
+  * the NT/NN/TN/TT storage layouts and D = C + A @ B.T with FP32 C and D
+    (README "Interface / Notes": SM100 supports all four layouts).
+  * the K-grouped GEMM of MoE weight gradients and its per-group scale pack
+    (README "News" 2025.05.14 and API list: k_grouped_fp8_gemm_tn_contiguous,
+    get_k_grouped_mn_major_tma_aligned_packed_ue8m0_tensor).
+  * per-token 1x128 FP8 quantisation writing packed scales (README "Interface /
+    Notes": quantisation is left to the caller, to be fused into a producer).
 
 Readings where the pages are silent (each listed in the design notes):
   P2  byte j of packed word kp holds K block 4*kp + j (little-endian).
@@ -35,6 +42,11 @@ Readings where the pages are silent (each listed in the design notes):
   P7  the exact sum is rounded once to BF16, round-to-nearest-even.
   P8  contiguous-layout padding rows (m_indices == -1) come out as +0.0.
   P9  masked-layout rows at or past masked_m[g] keep whatever D held before.
+  P13 C is added to the exact product sum and the result rounded once (to FP32
+      or BF16); the GPU adds C to its FP32 accumulator, one more rounding.
+  P14 K-grouped scales: one FP32 scale per 128-row K block and per column of the
+      MN-major operand ([sum Kb][MN]), packed per group so that no packed word
+      spans two groups; every ks[g] is a multiple of 128.
   P1  (per-token quantisation) the scale of a 1x128 block is 2**e with e the smallest integer
       such that 448 * 2**e >= amax, clamped to [-127, 127], 0 for an all-zero block.
 """
@@ -43,4 +55,5 @@ from .reference import (  # noqa: F401
     pack_sf_ue8m0, unpack_sf_ue8m0, bf16_round_bits, bf16_bits_to_float,
     fp8_gemm_nt, fp8_gemm_nt_unrounded, m_grouped_fp8_gemm_nt_contiguous,
     m_grouped_fp8_gemm_nt_masked, e4m3_encode_rne, block_scale_exponent, quantize_fp8_1x128,
+    f32_round, fp8_gemm, k_group_offsets, pack_sf_ue8m0_k_grouped, k_grouped_fp8_gemm_tn_contiguous,
 )

@@ -315,3 +315,101 @@ def quantize_fp8_1x128(x: np.ndarray):
     codes = e4m3_encode_rne(scaled).reshape(M, K)
     packed = pack_sf_ue8m0(np.ldexp(1.0, e).astype(np.float32), M, 1)[0]
     return codes, packed
+
+
+# ---------------------------------------------------------------------------
+# Memory layouts and FP32 accumulation (README "Interface / Notes": the SM100 kernels take
+# the NT, TN, NN and TT layouts and compute D = C + A @ B.T)
+# ---------------------------------------------------------------------------
+
+def f32_round(x: np.ndarray) -> np.ndarray:
+    """float64 -> float32, one round-to-nearest-even step (numpy's conversion)."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32)
+
+
+def _k_major(codes: np.ndarray, stored_mn_major: bool) -> np.ndarray:
+    """An operand as [rows, K] codes: an MN-major operand is stored [K, rows]."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    return np.ascontiguousarray(codes.T) if stored_mn_major else codes
+
+
+def fp8_gemm(a_codes, sfa_packed, b_codes, sfb_packed, layout: str = "nt", c=None, out: str = "bf16"):
+    """D = C + A @ B^T for the four storage layouts, rounded once to BF16 bits or FP32.
+
+    layout[0] is A's letter: 'n' = stored [M, K] (K contiguous), 't' = stored [K, M].
+    layout[1] is B's letter: 't' = stored [N, K] (K contiguous), 'n' = stored [K, N].
+    The scale tensors do not depend on the layout: word [kp][r] of sfa covers row m = r of
+    D's rows, of sfb row n = r.  c (optional) is FP32 [M, N], added exactly before rounding.
+    """
+    assert layout in ("nt", "nn", "tn", "tt") and out in ("bf16", "f32")
+    a = _k_major(a_codes, layout[0] == "t")
+    b = _k_major(b_codes, layout[1] == "n")
+    d = fp8_gemm_nt_unrounded(a, sfa_packed, b, sfb_packed)
+    if c is not None:
+        d = d + np.asarray(c, dtype=np.float32).astype(np.float64)
+    return bf16_round_bits(d) if out == "bf16" else f32_round(d)
+
+
+# ---------------------------------------------------------------------------
+# K-grouped GEMM for MoE weight gradients (README "News" 2025.05.14 and the API list:
+# k_grouped_fp8_gemm_tn_contiguous, get_k_grouped_mn_major_tma_aligned_packed_ue8m0_tensor)
+# ---------------------------------------------------------------------------
+
+def k_group_offsets(ks):
+    """Per group: first K row, first K block and first packed-word row (exclusive prefix sums
+    of ks, ks / 128 and ceil(ks / 512)); each ks[g] is a multiple of 128."""
+    ks = np.asarray(ks, dtype=np.int64)
+    assert np.all(ks >= 0) and np.all(ks % BLOCK_K == 0)
+    kb = ks // BLOCK_K
+    kp = (kb + 3) // 4
+    excl = lambda v: np.concatenate([[0], np.cumsum(v)[:-1]]).astype(np.int64)
+    return excl(ks), excl(kb), excl(kp)
+
+
+def pack_sf_ue8m0_k_grouped(sf: np.ndarray, mn: int, ks) -> np.ndarray:
+    """float sf [sum_g ks[g]/128][mn] (one scale per K block and row, MN contiguous) ->
+    int32 [sum_g ceil(ks[g]/512)][al4(mn)].
+
+    Each group is packed on its own: word row kpoff[g] + j, byte i holds the UE8M0 code of
+    the scale of the group's K block 4j + i (0 past the group's last block); rows >= mn are 0.
+    """
+    sf = np.asarray(sf, dtype=np.float32)
+    ks = np.asarray(ks, dtype=np.int64)
+    _, kboff, _ = k_group_offsets(ks)
+    parts = []
+    for g in range(ks.size):
+        kb_g = int(ks[g]) // BLOCK_K
+        if kb_g == 0:
+            continue
+        per_row = sf[kboff[g]:kboff[g] + kb_g, :mn].T                 # [mn, Kb_g]
+        parts.append(pack_sf_ue8m0(per_row[None], mn, 1)[0])
+    if not parts:
+        return np.zeros((0, tma_aligned_size(mn, 4)), dtype=np.int32)
+    return np.concatenate(parts, axis=0)
+
+
+def k_grouped_fp8_gemm_tn_contiguous(a_codes, sfa_packed, b_codes, sfb_packed, ks, c=None) -> np.ndarray:
+    """FP32 [G, M, N]: D[g] = C[g] + sum over the K rows k of group g of A[k, :]^T B[k, :].
+
+    a_codes [sum K, M] and b_codes [sum K, N] are MN-major (the 't' A and 'n' B layouts);
+    group g owns K rows koff[g] .. koff[g] + ks[g].  sfa_packed [sum Kp_g][al4(M)] and
+    sfb_packed [sum Kp_g][al4(N)] hold per-row scales of 1x128 K blocks, packed per group
+    (`pack_sf_ue8m0_k_grouped`).  A group with ks[g] = 0 gives D[g] = C[g] (0 without C).
+    """
+    a_codes = np.asarray(a_codes, dtype=np.uint8)
+    b_codes = np.asarray(b_codes, dtype=np.uint8)
+    ks = np.asarray(ks, dtype=np.int64)
+    M, N = a_codes.shape[1], b_codes.shape[1]
+    koff, _, kpoff = k_group_offsets(ks)
+    out = np.zeros((ks.size, M, N), dtype=np.float32)
+    for g in range(ks.size):
+        d = np.zeros((M, N), dtype=np.float64)
+        if ks[g] > 0:
+            rows = slice(koff[g], koff[g] + ks[g])
+            kp = (int(ks[g]) // BLOCK_K + 3) // 4
+            words = slice(kpoff[g], kpoff[g] + kp)
+            d = fp8_gemm_nt_unrounded(a_codes[rows].T, sfa_packed[words], b_codes[rows].T, sfb_packed[words])
+        if c is not None:
+            d = d + np.asarray(c[g], dtype=np.float32).astype(np.float64)
+        out[g] = f32_round(d)
+    return out

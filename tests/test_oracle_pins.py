@@ -476,3 +476,91 @@ def test_quantize_agrees_with_the_input_generator_on_bf16_activations():
     s_codes, s_sf = synth.quantize_1x128(xf.astype(np.float32))
     assert np.array_equal(codes, s_codes)
     assert np.array_equal(packed, oracle.pack_sf_ue8m0(s_sf, 6, 1)[0])
+
+
+# ---------------------------------------------------------------------------
+# Layouts, FP32 accumulation, K-grouped GEMM: brute force on tiny inputs, from the FP32 scales
+# (not the packed words) and with torch's E4M3 decode, one product at a time.
+# ---------------------------------------------------------------------------
+
+def _finite_codes(rs, shape):
+    c = rs.integers(0, 256, size=shape).astype(np.uint8)
+    return np.where((c & 0x7F) == 0x7F, c ^ 0x01, c).astype(np.uint8)      # no NaN codes
+
+
+def _dec(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).double().numpy()
+
+
+@pytest.mark.parametrize("layout", ["nt", "nn", "tn", "tt"])
+def test_fp8_gemm_layouts_and_accumulation_brute_force(layout):
+    rs = np.random.default_rng(31)
+    M, N, K = 3, 5, 256
+    a = _finite_codes(rs, (M, K))                      # logical A[m, k]
+    b = _finite_codes(rs, (N, K))                      # logical B[n, k]
+    sa = np.ldexp(np.float32(1), rs.integers(-6, 7, (M, 2))).astype(np.float32)
+    sb = np.ldexp(np.float32(1), rs.integers(-6, 7, (N, 2))).astype(np.float32)
+    c = rs.standard_normal((M, N)).astype(np.float32)
+    a_st = a if layout[0] == "n" else np.ascontiguousarray(a.T)
+    b_st = b if layout[1] == "t" else np.ascontiguousarray(b.T)
+    got = oracle.fp8_gemm(a_st, oracle.pack_sf_ue8m0(sa, M, 1)[0], b_st, oracle.pack_sf_ue8m0(sb, N, 1)[0],
+                          layout=layout, c=c, out="f32")
+    av, bv = _dec(a), _dec(b)
+    for m in range(M):
+        for n in range(N):
+            terms = [float(c[m, n])]
+            for k in range(K):
+                terms.append(av[m, k] * bv[n, k] * float(sa[m, k // 128]) * float(sb[n, k // 128]))
+            assert got[m, n] == np.float32(math.fsum(terms)), (layout, m, n)
+
+
+def test_k_grouped_pack_brute_force():
+    rs = np.random.default_rng(32)
+    ks = [128, 0, 640, 384, 512]
+    mn = 6
+    kb_total = sum(ks) // 128
+    sf = np.ldexp(np.float32(1), rs.integers(-20, 21, (kb_total, mn))).astype(np.float32)
+    packed = oracle.pack_sf_ue8m0_k_grouped(sf, mn, ks).view(np.uint32)
+    assert packed.shape == (1 + 0 + 2 + 1 + 1, 8)
+    row = 0
+    blk = 0
+    for kg in ks:
+        nb = kg // 128
+        for w in range((nb + 3) // 4):
+            for r in range(8):
+                for i in range(4):
+                    byte = (int(packed[row + w, r]) >> (8 * i)) & 0xFF
+                    j = 4 * w + i
+                    if r >= mn or j >= nb:
+                        assert byte == 0
+                    else:
+                        assert byte == math.frexp(float(sf[blk + j, r]))[1] - 1 + 127
+        row += (nb + 3) // 4
+        blk += nb
+
+
+def test_k_grouped_gemm_brute_force():
+    rs = np.random.default_rng(33)
+    ks = [128, 0, 256]
+    M, N = 3, 4
+    Kt = sum(ks)
+    a = _finite_codes(rs, (Kt, M))                     # MN-major: [K, M]
+    b = _finite_codes(rs, (Kt, N))
+    sa = np.ldexp(np.float32(1), rs.integers(-5, 6, (Kt // 128, M))).astype(np.float32)
+    sb = np.ldexp(np.float32(1), rs.integers(-5, 6, (Kt // 128, N))).astype(np.float32)
+    c = rs.standard_normal((len(ks), M, N)).astype(np.float32)
+    got = oracle.k_grouped_fp8_gemm_tn_contiguous(a, oracle.pack_sf_ue8m0_k_grouped(sa, M, ks), b,
+                                                  oracle.pack_sf_ue8m0_k_grouped(sb, N, ks), ks, c=c)
+    av, bv = _dec(a), _dec(b)
+    k0 = 0
+    for g, kg in enumerate(ks):
+        for m in range(M):
+            for n in range(N):
+                terms = [float(c[g, m, n])]
+                for k in range(k0, k0 + kg):
+                    terms.append(av[k, m] * bv[k, n] * float(sa[k // 128, m]) * float(sb[k // 128, n]))
+                assert got[g, m, n] == np.float32(math.fsum(terms)), (g, m, n)
+        k0 += kg
+    no_c = oracle.k_grouped_fp8_gemm_tn_contiguous(a, oracle.pack_sf_ue8m0_k_grouped(sa, M, ks), b,
+                                                   oracle.pack_sf_ue8m0_k_grouped(sb, N, ks), ks)
+    assert np.all(no_c[1] == 0) and no_c[1].tobytes() == np.zeros((M, N), np.float32).tobytes()
