@@ -410,6 +410,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                       "stream, scale pack + GEMM on the compute stream, D copied back on a third stream, "
                       "overlapped across workloads; weights resident"}
 
+    next_rows = None if args.no_next else time_next_rows(dev, peaks)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = time_oracle(ws, budget_s=args.cpu_budget, rows_per_workload=1024)
@@ -427,8 +429,50 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                          "streams ~1 GB (> 129 MB L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks, "workloads": per_wl,
+        "clocks": clocks, "workloads": per_wl, "next_rows": next_rows,
     }
+
+
+# Kernels beyond the GEMM step, each timed alone on its own workload (not part of `value`).
+NEXT_QUANTIZE = [("quantize_32768x7168_bf16", 32768, 7168),     # the contiguous MoE tokens
+                 ("quantize_4096x16384_bf16", 4096, 16384)]     # the prefill A
+
+
+def time_next_rows(dev, peaks, reps: int = 20):
+    """Per-token 1x128 FP8 quantisation: ms per launch (median of `reps`, CUDA events on the
+    launching stream, L2 flushed before every rep), algorithmic bytes = 2 MK read + MK codes
+    + 4 Kp al4(M) scale bytes written."""
+    import moe_grouped_gemm_02_gb300 as dg
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)     # 256 MB > L2
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    rows = []
+    for name, M, K in NEXT_QUANTIZE:
+        x = torch.randn((M, K), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+        q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        sf = torch.empty(dg.packed_sf_shape(None, M, K), dtype=torch.int32, device=dev)
+        for _ in range(3):
+            dg.dg_quantize_fp8_1x128(x, q, sf)
+        ts = []
+        for r in range(reps):
+            flush.fill_(float(r))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dg.dg_quantize_fp8_1x128(x, q, sf)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        dg.dg_check_device_error()
+        ms = statistics.median(ts)
+        nbytes = 3 * M * K + 4 * sf.numel()
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows.append({"row": "per-token 1x128 FP8 quantisation (dg_quantize_fp8_1x128)", "workload": name,
+                     "ms": round(ms, 5), "ms_min": round(min(ts), 5), "ms_max": round(max(ts), 5),
+                     "bytes": nbytes, "gbs": round(gbs, 1), "bound": "hbm",
+                     "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm copy (of {peaks['source']})"})
+        del x, q, sf
+    return rows
 
 
 def time_oracle(ws, budget_s: float = 20.0, rows_per_workload: int = 4):
@@ -507,6 +551,7 @@ def main():
     ap.add_argument("--impl", default="dg", choices=["dg", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip the kernels timed beside the GEMM step")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "dg":
