@@ -121,6 +121,70 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
                                           const int32_t* sfb, void* d, const int32_t* masked_m,
                                           int G, int max_m, int N, int K, void* stream);
 
+/* Storage layouts of the operands of dg_fp8_gemm (README "Interface / Notes": the SM100 kernels
+ * take the NT, TN, NN and TT layouts).  The first letter is A's, the second B's:
+ *   A 'n': [M, K], K contiguous        A 't': [K, M], M contiguous (MN-major)
+ *   B 't': [N, K], K contiguous        B 'n': [K, N], N contiguous (MN-major)  */
+enum { DG_LAYOUT_NT = 0, DG_LAYOUT_NN = 1, DG_LAYOUT_TN = 2, DG_LAYOUT_TT = 3 };
+
+/*
+ * D = C + A @ B^T in any of the four layouts, BF16 or FP32 out (README "Interface / Notes":
+ * fp8_gemm_{nt, nn, tn, tt} compute D = C + A @ B.T).
+ *
+ *   a, b      E4M3, stored as `layout` says (see DG_LAYOUT_*)
+ *   sfa, sfb  packed UE8M0 scales exactly as for dg_fp8_gemm_nt: word [kp][m] covers row m of
+ *             D's rows and K blocks 4kp..4kp+3, word [kp][n] column n (the layout of the
+ *             operands does not change the scales' layout)
+ *   c         FP32 [M, N] or NULL; only with out_f32 = 1.  c may equal d (in-place
+ *             accumulation): each element of C is read before the same element of D is written
+ *   d         BF16 [M, N] (out_f32 = 0) or FP32 [M, N] (out_f32 = 1)
+ * Requires what dg_fp8_gemm_nt requires, plus M % 16 == 0 when A is MN-major and N % 16 == 0
+ * when B is MN-major (16-byte row pitch); c, when given, 16-byte aligned.
+ * C is added to the FP32 accumulator before the final rounding.  layout = DG_LAYOUT_NT with
+ * out_f32 = 0 and c = NULL is dg_fp8_gemm_nt.
+ */
+dg_status dg_fp8_gemm(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const float* c,
+                      void* d, int M, int N, int K, int layout, int out_f32, void* stream);
+
+/*
+ * K-grouped GEMM of MoE weight gradients (README "News" 2025.05.14 and the API list:
+ * k_grouped_fp8_gemm_tn_contiguous): for every group g,
+ *     D[g] = C[g] + A_g^T B_g,   A_g = rows koff[g] .. koff[g] + ks[g] of A, same for B,
+ * koff the exclusive prefix sum of ks.  Both operands are MN-major (the 't' A and 'n' B of
+ * the TN layout): the groups are consecutive row ranges of the shared K (token) dimension.
+ *
+ *   a     e4m3  [sum_K][M]   M contiguous
+ *   b     e4m3  [sum_K][N]   N contiguous
+ *   sfa   int32 [sum_g ceil(ks[g]/512)][al4(M)]   per-group packed scales of A's 1x128 K blocks
+ *   sfb   int32 [sum_g ceil(ks[g]/512)][al4(N)]   the same for B (dg_pack_sf_ue8m0_k_grouped)
+ *   c     float [G][M][N] or NULL (may equal d)
+ *   d     float [G][M][N]
+ *   ks    int32 [G], device memory: K rows per group, each a multiple of 128, summing to sum_K
+ *         (read on the device, so the call can be captured in a CUDA graph; checked only under
+ *         DG_VALIDATE=1, which returns DG_ERR_CONTRACT)
+ * A group with ks[g] = 0 gives D[g] = C[g] (zeros without C).  Requires G in 1..4096,
+ * M % 16 == 0, N % 16 == 0, sum_K % 128 == 0, 16-byte aligned pointers.  Group sizes summing
+ * past sum_K are clipped there (only rows of a and b below sum_K are read).
+ */
+dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                              const float* c, float* d, const int32_t* ks, int G, int M, int N,
+                                              int sum_K, void* stream);
+
+/*
+ * Per-group scale pack for the K-grouped GEMM (README API list:
+ * get_k_grouped_mn_major_tma_aligned_packed_ue8m0_tensor).
+ *
+ *   sf   float [sum_K / 128][MN]           one scale per 128-row K block and per column
+ *   out  int32 [sum_g ceil(ks[g]/512)][al4(MN)]
+ *   ks   int32 [G], device memory, as for dg_k_grouped_fp8_gemm_tn_contiguous
+ * Group g's word row kpoff[g] + j, byte i holds the UE8M0 code (the rounding-up rule of
+ * dg_pack_sf_ue8m0) of the scale of the group's K block 4j + i, 0 past its last block; no
+ * word spans two groups.  Padding columns [MN, al4(MN)) are 0.  Requires sum_K % 128 == 0 and
+ * sum_K / 512 + G <= 65535.
+ */
+dg_status dg_pack_sf_ue8m0_k_grouped(const float* sf, int32_t* out, const int32_t* ks, int G, int MN, int sum_K,
+                                     void* stream);
+
 /*
  * Scale-factor pack: FP32 scales -> MN-major, TMA-aligned, packed UE8M0
  * (README "Interface / Notes" and "Utilities": get_mn_major_tma_aligned_packed_ue8m0_tensor;

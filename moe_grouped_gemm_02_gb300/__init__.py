@@ -27,7 +27,10 @@ _STATUS = {0: "DG_OK", 1: "DG_ERR_INVALID_ARG", 2: "DG_ERR_SHAPE", 3: "DG_ERR_AL
 EXPORTS = ("dg_fp8_gemm_nt", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_grouped_fp8_gemm_nt_masked",
            "dg_pack_sf_ue8m0", "dg_get_mk_alignment_for_contiguous_layout", "dg_get_tma_aligned_size",
            "dg_set_num_sms", "dg_get_num_sms", "dg_set_pdl", "dg_get_pdl", "dg_status_string",
-           "dg_check_device_error", "dg_quantize_fp8_1x128")
+           "dg_check_device_error", "dg_quantize_fp8_1x128", "dg_fp8_gemm",
+           "dg_k_grouped_fp8_gemm_tn_contiguous", "dg_pack_sf_ue8m0_k_grouped")
+
+LAYOUTS = {"nt": 0, "nn": 1, "tn": 2, "tt": 3}
 
 
 class DGError(RuntimeError):
@@ -53,8 +56,12 @@ def load_library() -> ctypes.CDLL:
     lib.dg_m_grouped_fp8_gemm_nt_masked.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     lib.dg_pack_sf_ue8m0.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp]
     lib.dg_quantize_fp8_1x128.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+    lib.dg_fp8_gemm.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
+    lib.dg_k_grouped_fp8_gemm_tn_contiguous.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+    lib.dg_pack_sf_ue8m0_k_grouped.argtypes = [vp, vp, vp, i32, i32, i32, vp]
     for name in ("dg_fp8_gemm_nt", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_grouped_fp8_gemm_nt_masked",
-                 "dg_pack_sf_ue8m0", "dg_check_device_error", "dg_quantize_fp8_1x128"):
+                 "dg_pack_sf_ue8m0", "dg_check_device_error", "dg_quantize_fp8_1x128", "dg_fp8_gemm",
+                 "dg_k_grouped_fp8_gemm_tn_contiguous", "dg_pack_sf_ue8m0_k_grouped"):
         getattr(lib, name).restype = i32
     lib.dg_check_device_error.argtypes = [vp]
     lib.dg_get_mk_alignment_for_contiguous_layout.argtypes = []
@@ -131,6 +138,44 @@ def dg_fp8_gemm_nt(a, sfa, b, sfb, d, stream=None) -> None:
     N = b.shape[0]
     _check("dg_fp8_gemm_nt", load_library().dg_fp8_gemm_nt(
         _ptr(a, "a"), _ptr(sfa, "sfa"), _ptr(b, "b"), _ptr(sfb, "sfb"), _ptr(d, "d"), M, N, K, _stream(stream)))
+
+
+def dg_fp8_gemm(a, sfa, b, sfb, d, layout: str = "nt", c=None, stream=None) -> None:
+    """d = c + a @ b^T in layout 'nt', 'nn', 'tn' or 'tt' (A 'n': [M, K], 't': [K, M];
+    B 't': [N, K], 'n': [K, N]); d BF16 (int16/bfloat16 storage) or float32, c float32 or None."""
+    a_t, b_n = layout[0] == "t", layout[1] == "n"
+    K, M = a.shape if a_t else a.shape[::-1]
+    N = b.shape[1] if b_n else b.shape[0]
+    out_f32 = 1 if d.dtype == torch.float32 else 0
+    cp = None if c is None else _ptr(c, "c")
+    _check("dg_fp8_gemm", load_library().dg_fp8_gemm(
+        _ptr(a, "a"), _ptr(sfa, "sfa"), _ptr(b, "b"), _ptr(sfb, "sfb"), cp, _ptr(d, "d"), M, N, K,
+        LAYOUTS[layout], out_f32, _stream(stream)))
+
+
+def dg_k_grouped_fp8_gemm_tn_contiguous(a, sfa, b, sfb, d, ks, c=None, stream=None) -> None:
+    """d[g] = c[g] + a_g^T @ b_g for the K row ranges of ks (device int32 [G]); a [sum_K, M],
+    b [sum_K, N], d and c float32 [G, M, N]."""
+    sum_K, M = a.shape
+    N = b.shape[1]
+    G = ks.shape[0]
+    cp = None if c is None else _ptr(c, "c")
+    _check("dg_k_grouped_fp8_gemm_tn_contiguous", load_library().dg_k_grouped_fp8_gemm_tn_contiguous(
+        _ptr(a, "a"), _ptr(sfa, "sfa"), _ptr(b, "b"), _ptr(sfb, "sfb"), cp, _ptr(d, "d"), _ptr(ks, "ks"),
+        G, M, N, sum_K, _stream(stream)))
+
+
+def dg_pack_sf_ue8m0_k_grouped(sf, out, ks, mn: int, stream=None) -> None:
+    """Packs float32 scales sf [sum_K/128][mn] per group (ks: device int32 [G]) into
+    out int32 [sum_g ceil(ks[g]/512)][al4(mn)]."""
+    _check("dg_pack_sf_ue8m0_k_grouped", load_library().dg_pack_sf_ue8m0_k_grouped(
+        _ptr(sf, "sf"), _ptr(out, "out"), _ptr(ks, "ks"), ks.shape[0], int(mn), sf.shape[0] * 128,
+        _stream(stream)))
+
+
+def k_grouped_packed_sf_rows(ks) -> int:
+    """Rows of a K-grouped packed scale tensor: sum over groups of ceil(ks[g] / 512)."""
+    return int(sum((int(k) // 128 + 3) // 4 for k in ks))
 
 
 def dg_m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, d, m_indices, stream=None) -> None:

@@ -168,7 +168,7 @@ int cluster_capacity(DeviceState& st, int cfg_index, const KernelConfig* c, int 
 }
 
 Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N, int kblocks, int sms,
-                 int extra_ints) {
+                 int extra_ints, int b_mn) {
     int n = 0;
     const KernelConfig* const* cfgs = all_configs(&n);
     const int ngroups = (kblocks + 3) / 4;
@@ -190,6 +190,10 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
             for (int split : {1, 2, 4, 8}) {
                 if (fsplit && split != fsplit) continue;
                 if (pair && split > 1) continue;
+                // MN-major B is loaded in boxes of 128 columns; K-grouped tiles have per-group K.
+                if (b_mn && c->bn % 128 != 0) continue;
+                if ((b_mn || mode == MODE_K_GROUPED) && pair) continue;
+                if (mode == MODE_K_GROUPED && split > 1) continue;
                 if (c->mh > 1 && (split > 1 || pair)) continue;
                 // Masked groups are filled to an unknown, typically partial, depth: 256-row tiles
                 // would mostly compute padding unless the groups are deep.
@@ -226,9 +230,32 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
     return best;
 }
 
-dg_status run_gemm(int mode, const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, void* d,
-                   const int32_t* m_indices, const int32_t* masked_m, int groups, int b_groups, int rows, int N,
-                   int K, void* stream) {
+// One GEMM call, as the entry points describe it.
+struct GemmCall {
+    int mode = MODE_DENSE;
+    const void* a = nullptr;
+    const int32_t* sfa = nullptr;
+    const void* b = nullptr;
+    const int32_t* sfb = nullptr;
+    void* d = nullptr;
+    const float* c = nullptr;       // FP32 C (out_f32 only)
+    int out_f32 = 0;
+    int a_mn = 0, b_mn = 0;         // operand stored MN-major
+    const int32_t* m_indices = nullptr;
+    const int32_t* masked_m = nullptr;
+    const int32_t* ks = nullptr;    // K-grouped: K rows per group
+    int groups = 1, b_groups = 1, rows = 0, N = 0, K = 0;
+};
+
+dg_status run_gemm(const GemmCall& call, void* stream) {
+    const int mode = call.mode;
+    const void* a = call.a;
+    const int32_t* sfa = call.sfa;
+    const void* b = call.b;
+    const int32_t* sfb = call.sfb;
+    const int32_t* m_indices = call.m_indices;
+    const int32_t* masked_m = call.masked_m;
+    const int groups = call.groups, b_groups = call.b_groups, rows = call.rows, N = call.N, K = call.K;
     DeviceState* st = nullptr;
     dg_status s = current_device(&st);
     if (s != DG_OK) return s;
@@ -276,28 +303,52 @@ dg_status run_gemm(int mode, const void* a, const int32_t* sfa, const void* b, c
                 return DG_ERR_CUDA;
             for (int g = 0; g < groups; ++g)
                 if (h[g] < 0 || h[g] > rows) return DG_ERR_CONTRACT;
+        } else if (mode == MODE_K_GROUPED) {
+            std::vector<int32_t> h(static_cast<size_t>(groups));
+            if (cudaMemcpy(h.data(), call.ks, h.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+                return DG_ERR_CUDA;
+            long long sum = 0;
+            for (int g = 0; g < groups; ++g) {
+                if (h[g] < 0 || h[g] % 128 != 0) return DG_ERR_CONTRACT;
+                sum += h[g];
+            }
+            if (sum != K) return DG_ERR_CONTRACT;
         }
     }
 
     const int sms = effective_sms(*st);
     const int m_blocks = (rows + 127) / 128;
     const int Kb = K / 128, Kp = (Kb + 3) / 4;
-    const int extra_ints = mode == MODE_MASKED ? groups + 1 : 0;
-    const Plan plan = choose_plan(*st, mode, rows, m_blocks * groups, N, Kb, sms, extra_ints);
-    if (!plan.cfg) return DG_ERR_SHAPE;   // nothing fits in shared memory (too many masked groups)
+    const bool kgrouped = mode == MODE_K_GROUPED;
+    const int extra_ints = mode == MODE_MASKED ? groups + 1 : (kgrouped ? 2 * (groups + 1) : 0);
+    // K-grouped: the plan sees the mean K of a group; scale words are packed per group, at most
+    // Kb / 4 + G rows in all (each group rounds its own count up).
+    const int plan_kb = kgrouped ? std::max(1, (Kb + groups - 1) / groups) : Kb;
+    const int kp_rows = kgrouped ? Kb / 4 + groups : Kp;
+    const Plan plan = choose_plan(*st, mode, rows, m_blocks * groups, N, plan_kb, sms, extra_ints, call.b_mn);
+    if (!plan.cfg) return DG_ERR_SHAPE;   // nothing fits in shared memory (too many groups)
     const KernelConfig* cfg = plan.cfg;
 
     CUtensorMap maps[4];
+    // A and D have one group per masked group; B one per expert (contiguous, masked).  K-grouped
+    // operands are single [sum K, MN] matrices whose groups are K ranges.
     const int a_groups = mode == MODE_MASKED ? groups : 1;
-    if (!encode_3d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, K, rows, a_groups, 128, 128 * cfg->mh,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_3d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, K, N, b_groups, 128,
-                   plan.pair ? cfg->bn / 2 : cfg->bn, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_3d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfa, al4(rows), Kp, a_groups, 128 * cfg->mh, 1,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_3d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfb, al4(N), Kp, b_groups, cfg->bn, 1,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
+    const int bz = kgrouped ? 1 : b_groups;
+    // (A K-grouped call with sum K = 0 loads nothing: its maps get a nominal extent.)
+    const int Km = K > 0 ? K : 128;
+    bool ok = call.a_mn ? encode_3d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, rows, Km, a_groups, 128, 128,
+                                    CU_TENSOR_MAP_SWIZZLE_128B)
+                        : encode_3d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, Km, rows, a_groups, 128,
+                                    128 * cfg->mh, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && (call.b_mn ? encode_3d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, N, Km, bz, 128, 128,
+                                      CU_TENSOR_MAP_SWIZZLE_128B)
+                          : encode_3d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, Km, N, bz, 128,
+                                      plan.pair ? cfg->bn / 2 : cfg->bn, CU_TENSOR_MAP_SWIZZLE_128B));
+    ok = ok && encode_3d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfa, al4(rows), kp_rows, a_groups,
+                         128 * cfg->mh, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok = ok && encode_3d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfb, al4(N), kp_rows, bz, cfg->bn, 1,
+                         CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok) return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
 
     GemmArgs args{};
     args.rows = rows;
@@ -311,7 +362,12 @@ dg_status run_gemm(int mode, const void* a, const int32_t* sfa, const void* b, c
     args.kblocks = Kb;
     args.m_indices = m_indices;
     args.masked_m = masked_m;
-    args.d = static_cast<uint16_t*>(d);
+    args.ks = call.ks;
+    args.a_mn = call.a_mn;
+    args.b_mn = call.b_mn;
+    args.out_f32 = call.out_f32;
+    args.c = call.c;
+    args.d = call.d;
     args.err = st->err_ptr;
     // DG_TIMEOUT_MS shortens the bound on every barrier wait and DG_DEBUG_DROP_LOAD=n makes
     // the producer skip its n-th stage: together they let a test drive the timeout path.
@@ -334,16 +390,17 @@ dg_status run_gemm(int mode, const void* a, const int32_t* sfa, const void* b, c
         args.raster_n = args.num_m_units >= 16 ? (args.num_n_blocks < 8 ? args.num_n_blocks : 8) : args.num_n_blocks;
     }
     args.num_units = mode == MODE_MASKED ? 0 : static_cast<int>(units_upper * passes);
+    if (units_upper * passes >= (1ll << 31)) return DG_ERR_SHAPE;
     args.split = plan.split;
     // Persistent grid: one CTA (or one cluster) per co-resident slot.
     const long long slots = units_upper < plan.capacity ? units_upper : plan.capacity;
     const int grid = static_cast<int>(slots) * (plan.split > 1 ? plan.split : (plan.pair ? 2 : 1));
     if (env_flag("DG_PRINT_CONFIGS"))
         std::fprintf(stderr,
-                     "[dg] mode=%d groups=%d rows=%d N=%d K=%d -> %s (BN=%d stages=%d acc=%d mh=%d) split=%d pair=%d "
-                     "grid=%d raster_n=%d\n",
-                     mode, groups, rows, N, K, cfg->name, cfg->bn, cfg->stages, cfg->acc, cfg->mh, plan.split,
-                     plan.pair, grid, args.raster_n);
+                     "[dg] mode=%d groups=%d rows=%d N=%d K=%d a_mn=%d b_mn=%d f32=%d -> %s (BN=%d stages=%d acc=%d "
+                     "mh=%d) split=%d pair=%d grid=%d raster_n=%d\n",
+                     mode, groups, rows, N, K, call.a_mn, call.b_mn, call.out_f32, cfg->name, cfg->bn, cfg->stages,
+                     cfg->acc, cfg->mh, plan.split, plan.pair, grid, args.raster_n);
     if (grid <= 0) return DG_OK;
     const cudaError_t e = cfg->launch(maps, args, grid, cs);
     return e == cudaSuccess ? DG_OK : cuda_fail("kernel launch", e);
@@ -374,7 +431,10 @@ dg_status dg_fp8_gemm_nt(const void* a, const int32_t* sfa, const void* b, const
     if (static_cast<long long>(M) * K >= (1ll << 40) || static_cast<long long>(N) * K >= (1ll << 40))
         return DG_ERR_SHAPE;
     if (M == 0) return DG_OK;
-    return run_gemm(MODE_DENSE, a, sfa, b, sfb, d, nullptr, nullptr, 1, 1, M, N, K, stream);
+    GemmCall call;
+    call.a = a, call.sfa = sfa, call.b = b, call.sfb = sfb, call.d = d;
+    call.rows = M, call.N = N, call.K = K;
+    return run_gemm(call, stream);
 }
 
 dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
@@ -387,7 +447,12 @@ dg_status dg_m_grouped_fp8_gemm_nt_contiguous(const void* a, const int32_t* sfa,
     if (static_cast<long long>(M_sum) * K >= (1ll << 40) || static_cast<long long>(G) * N * K >= (1ll << 40))
         return DG_ERR_SHAPE;
     if (M_sum == 0) return DG_OK;
-    return run_gemm(MODE_CONTIGUOUS, a, sfa, b, sfb, d, m_indices, nullptr, 1, G, M_sum, N, K, stream);
+    GemmCall call;
+    call.mode = MODE_CONTIGUOUS;
+    call.a = a, call.sfa = sfa, call.b = b, call.sfb = sfb, call.d = d;
+    call.m_indices = m_indices;
+    call.b_groups = G, call.rows = M_sum, call.N = N, call.K = K;
+    return run_gemm(call, stream);
 }
 
 dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
@@ -400,7 +465,57 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
     if (static_cast<long long>(G) * max_m * K >= (1ll << 40) || static_cast<long long>(G) * N * K >= (1ll << 40))
         return DG_ERR_SHAPE;
     if (max_m == 0) return DG_OK;
-    return run_gemm(MODE_MASKED, a, sfa, b, sfb, d, nullptr, masked_m, G, G, max_m, N, K, stream);
+    GemmCall call;
+    call.mode = MODE_MASKED;
+    call.a = a, call.sfa = sfa, call.b = b, call.sfb = sfb, call.d = d;
+    call.masked_m = masked_m;
+    call.groups = G, call.b_groups = G, call.rows = max_m, call.N = N, call.K = K;
+    return run_gemm(call, stream);
+}
+
+dg_status dg_fp8_gemm(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, const float* c,
+                      void* d, int M, int N, int K, int layout, int out_f32, void* stream) {
+    if (M < 0 || layout < DG_LAYOUT_NT || layout > DG_LAYOUT_TT || (out_f32 != 0 && out_f32 != 1))
+        return DG_ERR_INVALID_ARG;
+    if (c && !out_f32) return DG_ERR_INVALID_ARG;
+    const dg_status s = check_common(a, sfa, b, sfb, d, N, K);
+    if (s != DG_OK) return s;
+    if (c && !aligned16(c)) return DG_ERR_ALIGNMENT;
+    const int a_mn = layout == DG_LAYOUT_TN || layout == DG_LAYOUT_TT;
+    const int b_mn = layout == DG_LAYOUT_NN || layout == DG_LAYOUT_TN;
+    // an MN-major operand's rows are M (or N) bytes long: TMA needs a 16-byte pitch
+    if ((a_mn && M % 16 != 0) || (b_mn && N % 16 != 0)) return DG_ERR_SHAPE;
+    if (static_cast<long long>(M) * K >= (1ll << 40) || static_cast<long long>(N) * K >= (1ll << 40))
+        return DG_ERR_SHAPE;
+    if (M == 0) return DG_OK;
+    GemmCall call;
+    call.a = a, call.sfa = sfa, call.b = b, call.sfb = sfb, call.d = d, call.c = c;
+    call.out_f32 = out_f32, call.a_mn = a_mn, call.b_mn = b_mn;
+    call.rows = M, call.N = N, call.K = K;
+    return run_gemm(call, stream);
+}
+
+dg_status dg_k_grouped_fp8_gemm_tn_contiguous(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                              const float* c, float* d, const int32_t* ks, int G, int M, int N,
+                                              int sum_K, void* stream) {
+    if (!a || !sfa || !b || !sfb || !d || !ks || G <= 0 || M < 0 || N <= 0 || sum_K < 0) return DG_ERR_INVALID_ARG;
+    if (G > kMaxMaskedGroups) return DG_ERR_SHAPE;
+    if (sum_K % 128 != 0 || M % 16 != 0 || N % 16 != 0) return DG_ERR_SHAPE;
+    if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(d) ||
+        (c && !aligned16(c)))
+        return DG_ERR_ALIGNMENT;
+    if (static_cast<long long>(M) * sum_K >= (1ll << 40) || static_cast<long long>(N) * sum_K >= (1ll << 40) ||
+        static_cast<long long>(G) * M * N >= (1ll << 40))
+        return DG_ERR_SHAPE;
+    if (M == 0) return DG_OK;
+    GemmCall call;
+    call.mode = MODE_K_GROUPED;
+    call.a = a, call.sfa = sfa, call.b = b, call.sfb = sfb, call.d = d, call.c = c;
+    call.out_f32 = 1, call.a_mn = 1, call.b_mn = 1;
+    call.ks = ks;
+    // sum_K == 0: every group is empty and D = C (or zeros); the kernel still runs to write it.
+    call.groups = G, call.rows = M, call.N = N, call.K = sum_K;
+    return run_gemm(call, stream);
 }
 
 dg_status dg_pack_sf_ue8m0(const float* sf, int32_t* out, int G, int MN, int K, int gran_mn, int gran_k,
@@ -432,6 +547,22 @@ dg_status dg_quantize_fp8_1x128(const void* x, void* q, int32_t* sf, int G, int 
     if (s != DG_OK) return s;
     const cudaError_t e = launch_quantize_fp8_1x128(x, q, sf, G, M, K, pdl_enabled(), static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidValue) return DG_ERR_SHAPE;
+    return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
+}
+
+dg_status dg_pack_sf_ue8m0_k_grouped(const float* sf, int32_t* out, const int32_t* ks, int G, int MN, int sum_K,
+                                     void* stream) {
+    if (!sf || !out || !ks || G <= 0 || MN < 0 || sum_K < 0) return DG_ERR_INVALID_ARG;
+    if (G > kMaxMaskedGroups || sum_K % 128 != 0) return DG_ERR_SHAPE;
+    if (!aligned16(out) || (reinterpret_cast<uintptr_t>(sf) & 3u)) return DG_ERR_ALIGNMENT;
+    const int kb_total = sum_K / 128;
+    if (kb_total / 4 + G > 65535) return DG_ERR_SHAPE;
+    if (MN == 0) return DG_OK;
+    DeviceState* st = nullptr;
+    const dg_status s = current_device(&st);
+    if (s != DG_OK) return s;
+    const cudaError_t e = launch_pack_sf_k_grouped(sf, out, ks, G, MN, al4(MN), kb_total, pdl_enabled(),
+                                                   static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DG_OK : DG_ERR_CUDA;
 }
 

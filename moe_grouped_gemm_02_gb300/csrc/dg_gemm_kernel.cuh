@@ -108,6 +108,10 @@ struct Unit {
     bool zero;      // nothing to compute (padding or an empty pass): write zeros / skip
     bool mc;        // pair mode: the two CTAs of the pair share B, loaded by multicast
     uint32_t hmask; // MH = 2: the 128-row halves computed in this unit
+    int kb_begin;   // K blocks [kb_begin, kb_end) of this unit (the CTA's split-K share, or
+    int kb_end;     //   the group's K blocks in K-grouped mode)
+    int koff;       // K-grouped: first K block of the group in A and B
+    int kpoff;      // K-grouped: first packed scale-word row of the group
 };
 
 // Unit u of the schedule.
@@ -120,10 +124,40 @@ struct Unit {
 //    pass 0.  If a tile's two halves belong to one expert, pass 0 computes both and pass 1 is
 //    empty; if they belong to two experts, pass h computes half h with that half's expert.
 template <int MH>
-__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cum, int u, uint32_t crank) {
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cum, int u, uint32_t crank, int kb0,
+                                            int kb1) {
     Unit t;
     t.mc = a.pair != 0;
     t.hmask = MH == 2 ? 3u : 1u;
+    t.kb_begin = kb0;
+    t.kb_end = kb1;
+    t.koff = 0;
+    t.kpoff = 0;
+    if (a.mode == MODE_K_GROUPED) {
+        // Group-major; within a group, raster bands as in the dense mode.  cum[0..G] are the
+        // groups' first K blocks, cum[G+1..2G+1] their first packed scale-word rows.
+        const int per_group = a.num_m_units * a.num_n_blocks;
+        const int g = u / per_group;
+        const int r0 = u - g * per_group;
+        const int per_band = a.num_m_units * a.raster_n;
+        const int band = r0 / per_band;
+        const int r = r0 - band * per_band;
+        const int n0 = band * a.raster_n;
+        const int width = min(a.raster_n, a.num_n_blocks - n0);
+        t.mb = r / width;
+        t.nb = n0 + (r - t.mb * width);
+        t.g = g;
+        t.gb = g;
+        // K ranges are clipped to the call's K extent, so that group sizes summing past it
+        // (a broken contract) still only read the operands' own rows.
+        const int c0 = min(cum[g], a.kblocks), c1 = min(cum[g + 1], a.kblocks);
+        t.koff = c0;
+        t.kb_begin = 0;
+        t.kb_end = c1 - c0;
+        t.kpoff = cum[a.groups + 1 + g];
+        t.zero = t.kb_end == 0;     // an empty group: D = C (or zeros)
+        return t;
+    }
     int pass = 0;
     if (MH == 2 && a.mode == MODE_CONTIGUOUS) {
         const int per_pass = a.num_units >> 1;
@@ -261,6 +295,70 @@ __device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
                  : "memory");
 }
 
+__device__ __forceinline__ void st_global_v4f(float* p, float4 v) {
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// Coherent load: C may alias D, which this kernel writes.
+__device__ __forceinline__ float4 ld_global_v4f(const float* p) {
+    float4 v;
+    asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p)
+                 : "memory");
+    return v;
+}
+
+// Stores columns [col, col + ncols) (ncols 32 or 16, clipped at N) of the output row that starts
+// at element `row_off` of D, from FP32 accumulator bits r: as BF16 (round to nearest even), or
+// as FP32 plus C when the call has one.  A zero row stores +0.0 (BF16) or C (FP32; 0 without C).
+__device__ __forceinline__ void store_row_chunk(const GemmArgs& args, size_t row_off, int col, int N,
+                                                const uint32_t (&r)[32], int ncols, bool zero_row) {
+    if (args.out_f32) {
+        float* drow = static_cast<float*>(args.d) + row_off;
+        const float* crow = args.c ? args.c + row_off : nullptr;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (4 * j < ncols && col + 4 * j < N) {
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (!zero_row)
+                    v = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                if (crow) {
+                    const float4 cv = ld_global_v4f(crow + col + 4 * j);
+                    v.x += cv.x;
+                    v.y += cv.y;
+                    v.z += cv.z;
+                    v.w += cv.w;
+                }
+                st_global_v4f(drow + col + 4 * j, v);
+            }
+        }
+    } else {
+        uint16_t* drow = static_cast<uint16_t*>(args.d) + row_off;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (8 * j < ncols && col + 8 * j < N) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (!zero_row) {
+                    v.x = pack_bf16x2(r[8 * j + 0], r[8 * j + 1]);
+                    v.y = pack_bf16x2(r[8 * j + 2], r[8 * j + 3]);
+                    v.z = pack_bf16x2(r[8 * j + 4], r[8 * j + 5]);
+                    v.w = pack_bf16x2(r[8 * j + 6], r[8 * j + 7]);
+                }
+                st_global_v4(drow + col + 8 * j, v);
+            }
+        }
+    }
+}
+
+// A row of a tile with nothing computed (padding, an empty K group): columns [c0, c1).
+__device__ __forceinline__ void store_zero_row(const GemmArgs& args, size_t row_off, int c0, int c1) {
+    uint32_t none[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) none[i] = 0u;
+    for (int c = c0; c < c1; c += 32) store_row_chunk(args, row_off, c, c1, none, 32, true);
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -354,13 +452,48 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (lane == 31) cum[G] = incl;
     }
+    if (args.mode == MODE_K_GROUPED && warp == 2) {
+        // cum[g] = sum over g' < g of ks[g'] / 128 (K blocks) and cum[G + 1 + g] the same sum of
+        // ceil(ks[g'] / 512) (packed scale-word rows): two exclusive warp scans over runs.
+        const int G = args.groups;
+        const int per = (G + 31) / 32;
+        const int g0 = min(G, static_cast<int>(lane) * per), g1 = min(G, g0 + per);
+        auto kb_of = [&](int g) { return max(__ldg(args.ks + g), 0) / BK; };
+        int run_kb = 0, run_kp = 0;
+        for (int g = g0; g < g1; ++g) {
+            run_kb += kb_of(g);
+            run_kp += (kb_of(g) + 3) / 4;
+        }
+        int incl_kb = run_kb, incl_kp = run_kp;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl_kb, off);
+            const int w = __shfl_up_sync(0xffffffffu, incl_kp, off);
+            if (lane >= static_cast<uint32_t>(off)) {
+                incl_kb += v;
+                incl_kp += w;
+            }
+        }
+        int acc_kb = incl_kb - run_kb, acc_kp = incl_kp - run_kp;
+        for (int g = g0; g < g1; ++g) {
+            cum[g] = acc_kb;
+            cum[G + 1 + g] = acc_kp;
+            acc_kb += kb_of(g);
+            acc_kp += (kb_of(g) + 3) / 4;
+        }
+        if (lane == 31) {
+            cum[G] = incl_kb;
+            cum[2 * G + 1] = incl_kp;
+        }
+    }
     tc_fence_before_sync();
     const bool clustered = split > 1 || pair;
-    // The producer needs nothing another warp prepares (except the masked-mode prefix sums),
+    // The producer needs nothing another warp prepares (except the masked and K-grouped
+    // prefix sums),
     // and outside pair mode it only writes its own CTA's shared memory: it arrives without
     // waiting and starts loading at once.  Everyone else waits for the barrier initialisation,
     // the TMEM address and, in a cluster, for every peer to be initialised.
-    const bool early_producer = warp == 0 && args.mode != MODE_MASKED && !pair;
+    const bool early_producer = warp == 0 && args.mode != MODE_MASKED && args.mode != MODE_K_GROUPED && !pair;
     if (clustered) {
         cluster_arrive();
         if (!early_producer) cluster_wait();
@@ -395,10 +528,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t sf_last_par = 0;
             bool ok = true;
             for (int u = u_first; ok && u < total_units; u += u_step) {
-                const Unit t = decode_unit<MH>(args, cum, u, crank);
+                const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
                 if (t.zero) continue;
                 const int ga = args.mode == MODE_MASKED ? t.g : 0;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
                     if ((kb & 3) == 0) {
                         // A new group of four K blocks: its packed scale words go to the next slot
                         // of the scale ring once the MMAs of the slot's previous group are done.
@@ -411,9 +544,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         sf_phbits ^= 1u << sf_slot;
                         const uint32_t sb = sffull_bar(sf_slot);
                         mbar_arrive_expect_tx(sb, C::TX_SF);
-                        tma_load_3d(base + C::OFF_SFA + sf_slot * C::SFA_BYTES, &tm_sfa, sb, t.mb * C::TM, kb >> 2, ga);
-                        tma_load_3d(base + C::OFF_SFB + sf_slot * C::SFB_BYTES, &tm_sfb, sb, t.nb * C::BN, kb >> 2,
-                                    t.gb);
+                        const int kp = t.kpoff + (kb >> 2);
+                        tma_load_3d(base + C::OFF_SFA + sf_slot * C::SFA_BYTES, &tm_sfa, sb, t.mb * C::TM, kp, ga);
+                        tma_load_3d(base + C::OFF_SFB + sf_slot * C::SFB_BYTES, &tm_sfb, sb, t.nb * C::BN, kp,
+                                    args.mode == MODE_K_GROUPED ? 0 : t.gb);
                         sf_last = sf_slot;
                         sf_last_par = par ^ 1u;
                         if (++sf_slot == C::SF_SLOTS) sf_slot = 0;
@@ -431,9 +565,26 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                     const uint32_t fb = full_bar(s);
                     mbar_arrive_expect_tx(fb, C::TX_AB);
-                    tma_load_3d(base + C::OFF_A + s * C::A_BYTES, &tm_a, fb, kb * BK, t.mb * C::TM, ga);
-                    if (!pair) {
-                        tma_load_3d(base + C::OFF_B + s * C::B_BYTES, &tm_b, fb, kb * BK, t.nb * C::BN, t.gb);
+                    const int kx = (t.koff + kb) * BK;
+                    const int gbz = args.mode == MODE_K_GROUPED ? 0 : t.gb;
+                    if (!args.a_mn) {
+                        tma_load_3d(base + C::OFF_A + s * C::A_BYTES, &tm_a, fb, kx, t.mb * C::TM, ga);
+                    } else {
+                        // MN-major A: one box of 128 rows x 128 K per 128-row half, 16 KB apart
+#pragma unroll
+                        for (int h = 0; h < MH; ++h)
+                            tma_load_3d(base + C::OFF_A + s * C::A_BYTES + h * (BM * BK), &tm_a, fb,
+                                        t.mb * C::TM + h * BM, kx, ga);
+                    }
+                    if (args.b_mn) {
+                        // MN-major B (BN a multiple of 128): one box of 128 columns x 128 K per
+                        // 128 columns, 16 KB apart (the descriptor's leading-dimension stride)
+#pragma unroll
+                        for (int j = 0; j < C::BN / 128; ++j)
+                            tma_load_3d(base + C::OFF_B + s * C::B_BYTES + j * (128 * BK), &tm_b, fb,
+                                        t.nb * C::BN + j * 128, kx, gbz);
+                    } else if (!pair) {
+                        tma_load_3d(base + C::OFF_B + s * C::B_BYTES, &tm_b, fb, kx, t.nb * C::BN, gbz);
                     } else {
                         // The B map's box is half a tile; with multicast each CTA of the pair loads
                         // one half into both CTAs, otherwise each loads both halves itself.
@@ -484,11 +635,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             bool ok = true;
             bool any_commit = false;
             uint32_t last_bar = 0, last_par = 0;
-            const uint64_t adesc0 = smem_desc_kmajor_sw128(base + C::OFF_A + h * (BM * BK));
-            const uint64_t bdesc0 = smem_desc_kmajor_sw128(base + C::OFF_B);
-            const uint32_t idesc0 = idesc_mxf8_e4m3(BM, C::BN, 0);
+            // K-major tiles advance 32 bytes (2 descriptor units) per MMA along K; MN-major tiles
+            // 32 rows of 128 bytes (256 units).
+            const uint64_t adesc0 = args.a_mn ? smem_desc_mnmajor_sw128(base + C::OFF_A + h * (BM * BK))
+                                              : smem_desc_kmajor_sw128(base + C::OFF_A + h * (BM * BK));
+            const uint64_t bdesc0 = args.b_mn ? smem_desc_mnmajor_sw128(base + C::OFF_B)
+                                              : smem_desc_kmajor_sw128(base + C::OFF_B);
+            const uint64_t astep = args.a_mn ? 256ull : 2ull;
+            const uint64_t bstep = args.b_mn ? 256ull : 2ull;
+            const uint32_t idesc0 = idesc_mxf8_e4m3(BM, C::BN, 0) | idesc_mn_major(args.a_mn, args.b_mn);
             for (int u = u_first; ok && u < total_units; u += u_step) {
-                const Unit t = decode_unit<MH>(args, cum, u, crank);
+                const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
                 if (t.zero) continue;
                 const bool active = (t.hmask >> h) & 1u;
                 if (!wait_fast(tempty_bar(acc), acc_ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_TMEM_EMPTY)) {
@@ -497,7 +654,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((acc * MH + h) * C::BN);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
                     if ((kb & 3) == 0) {
                         // First K block of a group: copy the group's re-laid scale words from its
                         // ring slot into this issuer's TMEM slot.  (The slot's previous MMAs are
@@ -533,12 +690,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
 #pragma unroll
                         for (int k = 0; k < BK / MMA_K; ++k)
-                            tc_mma_mxf8f6f4(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc, sfa_t, sfb_t,
-                                            (kb != kb0 || k != 0) ? 1u : 0u);
+                            tc_mma_mxf8f6f4(d_tmem, adesc + astep * k, bdesc + bstep * k, idesc, sfa_t, sfb_t,
+                                            (kb != t.kb_begin || k != 0) ? 1u : 0u);
                     }
                     if (pair) tc_commit_multicast(empty_bar(s), 0x3);
                     else tc_commit(empty_bar(s));
-                    if ((kb & 3) == 3 || kb == kb1 - 1) {
+                    if ((kb & 3) == 3 || kb == t.kb_end - 1) {
                         tc_commit(sfempty_bar(sf_slot));
                         if (++sf_slot == C::SF_SLOTS) sf_slot = 0;
                     }
@@ -567,9 +724,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         uint32_t sff_phbits = 0;
         bool ok = true;
         for (int u = u_first; ok && u < total_units; u += u_step) {
-            const Unit t = decode_unit<MH>(args, cum, u, crank);
+            const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
             if (t.zero) continue;
-            for (int kb = kb0; kb < kb1; kb += 4) {
+            for (int kb = t.kb_begin; kb < t.kb_end; kb += 4) {
                 if (!wait_fast(sffull_bar(sf_slot), (sff_phbits >> sf_slot) & 1u, misc + 1, args.err,
                                args.timeout_ns, SITE_SF_FULL)) {
                     ok = false;
@@ -601,7 +758,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         uint32_t red_fph = 0;  // split-K: parity of this warp's receive barrier (owning warps)
         for (int u = u_first; u < total_units; u += u_step) {
             if (misc[1]) break;
-            const Unit t = decode_unit<MH>(args, cum, u, crank);
+            const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
             if (t.zero && t.hmask == 0u) continue;     // an empty pass: nothing to write
             const int n0 = t.nb * C::BN;
             const int m_valid = args.mode == MODE_MASKED ? min(max(__ldg(args.masked_m + t.g), 0), args.rows)
@@ -616,8 +773,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     zero_row = (e < 0 || e >= args.b_groups);
                 }
             };
-            auto drow_of = [&](int row) {
-                return args.d + (static_cast<size_t>(t.g) * args.rows + row) * static_cast<size_t>(N);
+            auto roff_of = [&](int row) {
+                return (static_cast<size_t>(t.g) * args.rows + row) * static_cast<size_t>(N);
             };
             if (split > 1) {
                 // Reduce-scatter of the cluster's partial accumulators: rows [o * RPO, (o+1) * RPO)
@@ -627,7 +784,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int row = row_of(0);
                 bool write, zero_row;
                 row_state(row, write, zero_row);
-                uint16_t* drow = drow_of(row);
+                const size_t row_off = roff_of(row);
                 const uint32_t RPO = BM / static_cast<uint32_t>(split);
                 const uint32_t r_in_tile = q * 32u + lane;
                 const uint32_t owner = r_in_tile / RPO;
@@ -638,8 +795,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 // receiving warp index within an owner (RPO = 64: two warps per owner)
                 const uint32_t rw = (r_in_tile % RPO) / 32u;
                 if (t.zero) {
-                    if (recv_lane && write)
-                        for (int c = n0; c < min(N, n0 + C::BN); c += 8) st_global_v4(drow + c, make_uint4(0, 0, 0, 0));
+                    if (recv_lane && write) store_zero_row(args, row_off, n0, min(N, n0 + C::BN));
                     continue;
                 }
                 if (!wait_or_abort(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
@@ -699,20 +855,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             }
                         }
                         if (write) {
-                            const int col = n0 + 32 * c;
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                if (col + 8 * j < N) {
-                                    uint4 o = make_uint4(0, 0, 0, 0);
-                                    if (!zero_row) {
-                                        o.x = pack_bf16x2(__float_as_uint(v[8 * j + 0]), __float_as_uint(v[8 * j + 1]));
-                                        o.y = pack_bf16x2(__float_as_uint(v[8 * j + 2]), __float_as_uint(v[8 * j + 3]));
-                                        o.z = pack_bf16x2(__float_as_uint(v[8 * j + 4]), __float_as_uint(v[8 * j + 5]));
-                                        o.w = pack_bf16x2(__float_as_uint(v[8 * j + 6]), __float_as_uint(v[8 * j + 7]));
-                                    }
-                                    st_global_v4(drow + col + 8 * j, o);
-                                }
-                            }
+                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+                            store_row_chunk(args, row_off, n0 + 32 * c, N, r, 32, zero_row);
                         }
                     }
                 }
@@ -736,9 +881,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const int row = row_of(h);
                     bool write, zero_row;
                     row_state(row, write, zero_row);
-                    if (write)
-                        for (int c = n0; c < min(N, n0 + C::BN); c += 8)
-                            st_global_v4(drow_of(row) + c, make_uint4(0, 0, 0, 0));
+                    if (write) store_zero_row(args, roff_of(row), n0, min(N, n0 + C::BN));
                 }
                 continue;
             }
@@ -750,7 +893,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int row = row_of(h);
                 bool write, zero_row;
                 row_state(row, write, zero_row);
-                uint16_t* drow = drow_of(row);
+                const size_t row_off = roff_of(row);
                 const uint32_t t_row =
                     tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>((acc * MH + h) * C::BN);
 #pragma unroll 1
@@ -760,22 +903,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     if (half_chunk) tmem_ld_32x32b_x16(t_row + 32u * c, r);
                     else tmem_ld_32x32b_x32(t_row + 32u * c, r);
                     tmem_wait_ld();
-                    if (write) {
-                        const int col = n0 + 32 * c;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            if (col + 8 * j < N && !(half_chunk && j >= 2)) {
-                                uint4 v = make_uint4(0, 0, 0, 0);
-                                if (!zero_row) {
-                                    v.x = pack_bf16x2(r[8 * j + 0], r[8 * j + 1]);
-                                    v.y = pack_bf16x2(r[8 * j + 2], r[8 * j + 3]);
-                                    v.z = pack_bf16x2(r[8 * j + 4], r[8 * j + 5]);
-                                    v.w = pack_bf16x2(r[8 * j + 6], r[8 * j + 7]);
-                                }
-                                st_global_v4(drow + col + 8 * j, v);
-                            }
-                        }
-                    }
+                    if (write) store_row_chunk(args, row_off, n0 + 32 * c, N, r, half_chunk ? 16 : 32, zero_row);
                 }
             }
         epilogue_release:

@@ -8,17 +8,18 @@
 
 namespace dg {
 
-enum : int { MODE_DENSE = 0, MODE_CONTIGUOUS = 1, MODE_MASKED = 2 };
+enum : int { MODE_DENSE = 0, MODE_CONTIGUOUS = 1, MODE_MASKED = 2, MODE_K_GROUPED = 3 };
 
 // Timeout sites recorded in the device error word (bits 8..15), DG_ERR_TIMEOUT in bits 0..7.
 enum : int { SITE_EMPTY = 1, SITE_FULL = 2, SITE_TMEM_EMPTY = 3, SITE_TMEM_FULL = 4, SITE_SF_EMPTY = 5, SITE_RED_EMPTY = 6, SITE_RED_FULL = 7,
              SITE_SF_READY = 8, SITE_SF_FULL = 9 };
 
 struct GemmArgs {
-    int rows;           // rows of A and D per group: M (dense), M_sum (contiguous), max_m (masked)
-    int N, K;
+    int rows;           // rows of A and D per group: M (dense), M_sum (contiguous), max_m (masked),
+                        // M (K-grouped)
+    int N, K;           // K: the whole K extent (K-grouped: the sum over the groups)
     int mode;           // MODE_*
-    int groups;         // groups of A and D (masked: G; otherwise 1)
+    int groups;         // groups of A and D (masked and K-grouped: G; otherwise 1)
     int b_groups;       // groups of B (dense: 1; contiguous and masked: G)
     int num_m_blocks;   // ceil(rows / 128)
     int num_n_blocks;   // ceil(N / BN)
@@ -28,9 +29,14 @@ struct GemmArgs {
     int split;          // CTAs (a thread-block cluster) sharing one tile's K range: 1, 2 or 4
     int pair;           // 1: clusters of 2 CTAs on adjacent m-blocks share each B tile by TMA multicast
     int num_m_units;    // m-blocks, or m-block pairs when pair == 1 (dense and contiguous)
+    int a_mn;           // 1: A is stored MN-major ([K, rows], rows contiguous)
+    int b_mn;           // 1: B is stored MN-major ([K, N], N contiguous)
+    int out_f32;        // 1: D is FP32; 0: BF16
     const int32_t* m_indices;
     const int32_t* masked_m;
-    uint16_t* d;        // BF16 bit patterns
+    const int32_t* ks;  // K-grouped: K rows of each group (multiples of 128)
+    const float* c;     // FP32 C added to the accumulators (out_f32 only; may alias d), or null
+    void* d;            // BF16 bit patterns or FP32
     int* err;           // device error word
     unsigned long long timeout_ns;
     int debug_drop_stage;   // test hook: the producer skips this stage's loads (-1: never)
@@ -65,6 +71,8 @@ const KernelConfig& config_bn192_s3_m2();
 
 cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb, int Kb, int Kp,
                            int mn_al, int gran_mn, int pdl, cudaStream_t stream);
+cudaError_t launch_pack_sf_k_grouped(const float* sf, int32_t* out, const int32_t* ks, int G, int MN, int mn_al,
+                                     int kb_total, int pdl, cudaStream_t stream);
 cudaError_t launch_quantize_fp8_1x128(const void* x, void* q, int32_t* sf, int G, int M, int K, int pdl,
                                       cudaStream_t stream);
 

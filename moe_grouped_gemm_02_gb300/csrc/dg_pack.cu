@@ -58,4 +58,88 @@ cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb
     return cudaLaunchKernelEx(&cfg, pack_sf_kernel, sf, out, MN, MNb, Kb, Kp, mn_al, gran_mn);
 }
 
+// K-grouped pack: FP32 scales sf [sum_g Kb_g][MN] (one per K block of 128 rows and per column
+// of an MN-major operand) -> int32 [sum_g ceil(Kb_g / 4)][mn_al], each group packed on its own
+// (its first K block starts a new word).  (README "News" 2025.05.14 and API list:
+// get_k_grouped_mn_major_tma_aligned_packed_ue8m0_tensor.)  The group sizes are read on the
+// device: every CTA first forms the prefix sums of the groups' K blocks and word rows in shared
+// memory, then each thread fills one word; threads past the last group's rows write nothing.
+__global__ void __launch_bounds__(256) pack_sf_k_grouped_kernel(const float* __restrict__ sf, int32_t* __restrict__ out,
+                                                                const int32_t* __restrict__ ks, int G, int MN,
+                                                                int mn_al, int kb_total) {
+    extern __shared__ int pk[];          // [0, G]: first K block of each group; [G+1, 2G+1]: first word row
+    griddep_wait();
+    griddep_launch_dependents();
+    const int tid = threadIdx.x;
+    const int per = (G + 255) / 256;
+    const int g0 = min(G, tid * per), g1 = min(G, g0 + per);
+    // clip the groups to the call's K extent (a broken contract still reads only sf's rows)
+    auto kb_raw = [&](int g) { return max(__ldg(ks + g), 0) / 128; };
+    int run_kb = 0, run_kp = 0;
+    for (int g = g0; g < g1; ++g) {
+        run_kb += kb_raw(g);
+        run_kp += (kb_raw(g) + 3) / 4;
+    }
+    int* scan = pk + 2 * (G + 1);       // 2 x 256 ints of scratch
+    scan[tid] = run_kb;
+    scan[256 + tid] = run_kp;
+    __syncthreads();
+    for (int off = 1; off < 256; off <<= 1) {   // inclusive Hillis-Steele scan, 8 steps
+        const int a = tid >= off ? scan[tid - off] : 0;
+        const int b = tid >= off ? scan[256 + tid - off] : 0;
+        __syncthreads();
+        scan[tid] += a;
+        scan[256 + tid] += b;
+        __syncthreads();
+    }
+    int acc_kb = scan[tid] - run_kb, acc_kp = scan[256 + tid] - run_kp;
+    for (int g = g0; g < g1; ++g) {
+        pk[g] = acc_kb;
+        pk[G + 1 + g] = acc_kp;
+        acc_kb += kb_raw(g);
+        acc_kp += (kb_raw(g) + 3) / 4;
+    }
+    if (tid == 255) {
+        pk[G] = scan[255];
+        pk[2 * G + 1] = scan[511];
+    }
+    __syncthreads();
+
+    const int r = blockIdx.x * blockDim.x + tid;
+    const int w = blockIdx.y;
+    if (r >= mn_al || w >= pk[2 * G + 1]) return;
+    int lo = 0, hi = G - 1;                      // the group whose word rows hold w
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pk[G + 1 + mid] <= w) lo = mid; else hi = mid - 1;
+    }
+    const int kb0 = pk[lo];
+    const int kbn = min(pk[lo + 1], kb_total) - min(kb0, kb_total);
+    const int j = w - pk[G + 1 + lo];
+    uint32_t word = 0;
+    if (r < MN) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int kb = 4 * j + i;
+            if (kb < kbn) word |= ue8m0_code_ceil(__ldg(sf + static_cast<size_t>(kb0 + kb) * MN + r)) << (8 * i);
+        }
+    }
+    out[static_cast<size_t>(w) * mn_al + r] = static_cast<int32_t>(word);
+}
+
+cudaError_t launch_pack_sf_k_grouped(const float* sf, int32_t* out, const int32_t* ks, int G, int MN, int mn_al,
+                                     int kb_total, int pdl, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((mn_al + 255) / 256, kb_total / 4 + G, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(2 * (G + 1) + 512) * sizeof(int);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, pack_sf_k_grouped_kernel, sf, out, ks, G, MN, mn_al, kb_total);
+}
+
 }  // namespace dg

@@ -322,6 +322,14 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
     return smem_desc(saddr, 16, 1024, 2);
 }
 
+// MN-major operand tile made of 128 x 128-byte boxes (128 MN elements by 128 K rows, the
+// 128-byte swizzle), boxes 16 KB apart along MN: the leading-dimension offset is the stride
+// between 128-element MN groups, the stride offset the one between 8-row K groups (1024 bytes).
+// Moving 32 rows along K adds 4096 bytes (256 units) to the start-address field.
+__device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(uint32_t saddr) {
+    return smem_desc(saddr, 16384, 1024, 2);
+}
+
 // 32 rows x 16 bytes, unswizzled and contiguous (core matrices of 8 rows 128 bytes apart).
 __device__ __forceinline__ uint64_t smem_desc_sf_chunk(uint32_t saddr) {
     return smem_desc(saddr, 128, 128, 0);
@@ -330,6 +338,11 @@ __device__ __forceinline__ uint64_t smem_desc_sf_chunk(uint32_t saddr) {
 // Instruction descriptor for kind::mxf8f6f4 with E4M3 A and B, both K-major, UE8M0 scales,
 // FP32 accumulation: B scale byte id (bits 4-5), A/B formats (7-9, 10-12; E4M3 = 0),
 // N >> 3 (17-22), scale type UE8M0 (bit 23), M >> 4 (24-28), A scale byte id (29-30).
+// Instruction-descriptor bits 15 and 16: A, respectively B, is MN-major in shared memory.
+__host__ __device__ constexpr uint32_t idesc_mn_major(int a_mn, int b_mn) {
+    return (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
+}
+
 __host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(uint32_t M, uint32_t N, uint32_t sf_id) {
     return ((sf_id & 3u) << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | ((sf_id & 3u) << 29);
 }

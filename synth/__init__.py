@@ -191,6 +191,26 @@ def make_masked(G: int, max_m: int, N: int, K: int, seed: int = 0, masked_m=None
                 a=a_q, sfa=a_sf, b=b_q, sfb=b_sf)
 
 
+def make_k_grouped(M: int, N: int, ks, seed: int = 0, a_outliers: bool = True) -> dict:
+    """Inputs of the K-grouped (weight-gradient) GEMM: a [sum K, M] and b [sum K, N], both
+    MN-major, N(0,1) (a with 1% outliers x20), quantized per group in blocks of 128 K rows by
+    1 column: sfa [sum K / 128, M], sfb [sum K / 128, N] (FP32 powers of two)."""
+    ks = np.asarray(ks, dtype=np.int64)
+    assert np.all(ks % BLOCK == 0)
+    K = int(ks.sum())
+    a = normal((K, M), seed, "a")
+    if a_outliers:
+        add_outliers(a, seed)
+    b = normal((K, N), seed, "b")
+    # each K block of 128 rows lies inside one group (ks are multiples of 128), so quantising
+    # the transposed operands in 1x128 blocks along K is the per-group quantisation
+    a_q, a_sf = quantize_1x128(np.ascontiguousarray(a.T))
+    b_q, b_sf = quantize_1x128(np.ascontiguousarray(b.T))
+    return dict(kind="k_grouped", G=int(ks.size), M=M, N=N, K=K, ks=ks.astype(np.int32),
+                a=np.ascontiguousarray(a_q.T), sfa=np.ascontiguousarray(a_sf.T),
+                b=np.ascontiguousarray(b_q.T), sfb=np.ascontiguousarray(b_sf.T))
+
+
 SENTINEL_BF16 = 0x7FA5   # a NaN pattern used to pre-fill D where rows must stay untouched
 
 

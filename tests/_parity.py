@@ -43,3 +43,21 @@ def assert_within_tolerance(d_bits: np.ndarray, ref_bits: np.ndarray, what: str 
     assert diff <= GLOBAL_TOL, f"{what}: global diff {diff}"
     return dict(max_rel=float(np.max(err / np.maximum(np.abs(r), 1e-30))), diff=diff,
                 max_err_over_rms=float(np.max(err)) / max(rms, 1e-30))
+
+
+def assert_close_f32(got: np.ndarray, ref: np.ndarray, what: str = "") -> dict:
+    """The same per-element and global bounds, for FP32 results (ref: the oracle's FP32)."""
+    d = np.asarray(got, dtype=np.float64).ravel()
+    r = np.asarray(ref, dtype=np.float64).ravel()
+    assert np.all(np.isfinite(d)), f"{what}: non-finite values in the GPU result"
+    if d.size == 0:
+        return {}
+    rms = float(np.sqrt(np.mean(r * r)))
+    err = np.abs(d - r)
+    bad = np.nonzero(err > REL_TOL * np.abs(r) + RMS_TOL * rms)[0]
+    assert bad.size == 0, (f"{what}: {bad.size} of {d.size} elements out of tolerance; first at flat "
+                           f"{bad[:5]}: got {d[bad[:5]]}, want {r[bad[:5]]}, rms {rms}")
+    den = float(np.sum(d * d + r * r))
+    diff = 1.0 - 2.0 * float(np.sum(d * r)) / den if den > 0 else 0.0
+    assert diff <= GLOBAL_TOL, f"{what}: global diff {diff}"
+    return dict(max_err_over_rms=float(np.max(err)) / max(rms, 1e-30), diff=diff)
