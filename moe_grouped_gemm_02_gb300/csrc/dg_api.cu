@@ -191,9 +191,12 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                 if (fsplit && split != fsplit) continue;
                 if (pair && split > 1) continue;
                 // MN-major B is loaded in boxes of 128 columns; K-grouped tiles have per-group K.
-                if (b_mn && c->bn % 128 != 0) continue;
+                if (b_mn && c->bn % 128 != 0 && c->mh != 2) continue;
                 if ((b_mn || mode == MODE_K_GROUPED) && pair) continue;
                 if (mode == MODE_K_GROUPED && split > 1) continue;
+                // one 128-row half with one accumulator: the epilogue warps split the columns,
+                // which the split-K reduction does not support
+                if (split > 1 && c->mh == 1 && c->acc == 1 && c->bn % 64 == 0) continue;
                 if (c->mh > 1 && (split > 1 || pair)) continue;
                 // Masked groups are filled to an unknown, typically partial, depth: 256-row tiles
                 // would mostly compute padding unless the groups are deep.
@@ -212,7 +215,9 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                 const long long tiles = m_units * ((N + c->bn - 1) / c->bn);
                 const long long waves = (tiles + cap - 1) / cap;
                 const double kb_per = 4.0 * ((ngroups + split - 1) / split);
-                const double tma = 2.2 * (128.0 * c->mh + (pair ? c->bn / 2 : c->bn));
+                // an MN-major B arrives in whole 128-column boxes
+                const double b_rows = b_mn ? 128.0 * ((c->bn + 127) / 128) : (pair ? c->bn / 2 : c->bn);
+                const double tma = 2.2 * (128.0 * c->mh + b_rows);
                 // one issuer: max(161, N/2 + 33) per MMA; two issuers (MH = 2) keep the pipe at N/2 + 33
                 const double mma = c->mh == 2 ? 8.0 * (c->bn / 2.0 + 33.0) : 4.0 * std::max(161.0, c->bn / 2.0 + 33.0);
                 const double t_tile = kb_per * (std::max(tma, mma) + 20.0) + 3000.0 + (split > 1 ? 1500.0 : 0.0);

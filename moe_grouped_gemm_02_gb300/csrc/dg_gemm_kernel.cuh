@@ -54,14 +54,23 @@ struct GemmCfg {
     static constexpr int TM = BM * MH;                  // rows of a tile
     // warps: producer, MMA issuer, 4 epilogue, scale re-layout (MH = 1); plus a second issuer
     // and 4 more epilogue warps, one set per 128-row half (MH = 2)
-    static constexpr int THREADS = MH == 2 ? 384 : 224;
-    static constexpr int EPI_THREADS = 128 * MH;
+    // With one 128-row half and one accumulator, the MMAs of the next tile wait for the
+    // epilogue to drain TMEM: two sets of four epilogue warps then split the tile's columns.
+    static constexpr int EPI_COLS = (MH == 1 && ACC_ == 1 && BN_ % 64 == 0) ? 2 : 1;
+    static constexpr int THREADS = (MH == 2 || EPI_COLS == 2) ? 384 : 224;
+    static constexpr int EPI_THREADS = 128 * MH * EPI_COLS;
     static_assert(MH == 1 || MH == 2, "a tile has one or two 128-row halves");
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 16 in [32, 256]");
     static_assert(BN % 32 == 0 || (ACC == 1 && MH == 1), "accumulators must start on 32-column boundaries");
     static constexpr int SFB_CHUNKS = (BN + 127) / 128;   // 128-row scale chunks of a B tile
     static constexpr int A_BYTES = TM * BK;
     static constexpr int B_BYTES = BN * BK;
+    // An MN-major B tile arrives in boxes of 128 columns (the 128-byte swizzle span): with
+    // MH = 2 the stage holds whole boxes, so that BN = 224 or 192 take an MN-major B too (the
+    // columns past BN are loaded and not used).  With MH = 1 only BN % 128 == 0 does.
+    static constexpr int B_BOXES = (BN + 127) / 128;
+    static constexpr int B_STAGE = MH == 2 ? B_BOXES * 128 * BK : B_BYTES;
+    static constexpr bool B_MN_OK = MH == 2 || BN % 128 == 0;
     static constexpr int SFA_BYTES = MH * 512;
     static constexpr int SFB_BYTES = SFB_CHUNKS * 512;
     static constexpr uint32_t TX_AB = A_BYTES + B_BYTES;
@@ -78,7 +87,7 @@ struct GemmCfg {
     // Shared memory, from a 1024-byte aligned base.
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-    static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_STAGE;
     static constexpr int OFF_SFB = OFF_SFA + SF_SLOTS * SFA_BYTES;
     static constexpr int OFF_BAR = OFF_SFB + SF_SLOTS * SFB_BYTES;
     // full/empty per stage; tmem full/empty per accumulator; sf full/ready/empty per scale
@@ -308,11 +317,23 @@ __device__ __forceinline__ float4 ld_global_v4f(const float* p) {
     return v;
 }
 
+// The C values of columns [col, col + ncols) (clipped at N) of the row at `row_off`, loaded
+// ahead of their use.
+__device__ __forceinline__ void load_c_chunk(const GemmArgs& args, size_t row_off, int col, int N, int ncols,
+                                             float4 (&cv)[8]) {
+    const float* crow = args.c + row_off;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (4 * j < ncols && col + 4 * j < N) cv[j] = ld_global_v4f(crow + col + 4 * j);
+}
+
 // Stores columns [col, col + ncols) (ncols 32 or 16, clipped at N) of the output row that starts
 // at element `row_off` of D, from FP32 accumulator bits r: as BF16 (round to nearest even), or
-// as FP32 plus C when the call has one.  A zero row stores +0.0 (BF16) or C (FP32; 0 without C).
+// as FP32 plus C when the call has one (cpre: C already loaded by load_c_chunk, else loaded
+// here).  A zero row stores +0.0 (BF16) or C (FP32; 0 without C).
 __device__ __forceinline__ void store_row_chunk(const GemmArgs& args, size_t row_off, int col, int N,
-                                                const uint32_t (&r)[32], int ncols, bool zero_row) {
+                                                const uint32_t (&r)[32], int ncols, bool zero_row,
+                                                const float4* cpre = nullptr) {
     if (args.out_f32) {
         float* drow = static_cast<float*>(args.d) + row_off;
         const float* crow = args.c ? args.c + row_off : nullptr;
@@ -324,7 +345,7 @@ __device__ __forceinline__ void store_row_chunk(const GemmArgs& args, size_t row
                     v = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                     __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
                 if (crow) {
-                    const float4 cv = ld_global_v4f(crow + col + 4 * j);
+                    const float4 cv = cpre ? cpre[j] : ld_global_v4f(crow + col + 4 * j);
                     v.x += cv.x;
                     v.y += cv.y;
                     v.z += cv.z;
@@ -384,7 +405,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     auto sffull_bar = [&](int j) { return base + C::OFF_BAR + 8u * (SFB0 + 2 * C::SF_SLOTS + j); };
     auto redfull_bar = [&](int j) { return base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + j); };
     const uint32_t redempty_bar = base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + 4);
-    const int split = MH == 1 ? args.split : 1;
+    const int split = (MH == 1 && C::EPI_COLS == 1) ? args.split : 1;
     const int pair = MH == 1 ? args.pair : 0;
     const uint32_t recv_base = base + C::off_recv(args.mode == MODE_MASKED ? args.groups + 1 : 0);
 
@@ -564,7 +585,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         continue;
                     }
                     const uint32_t fb = full_bar(s);
-                    mbar_arrive_expect_tx(fb, C::TX_AB);
+                    mbar_arrive_expect_tx(fb, args.b_mn ? C::A_BYTES + C::B_BOXES * 128 * BK : C::TX_AB);
                     const int kx = (t.koff + kb) * BK;
                     const int gbz = args.mode == MODE_K_GROUPED ? 0 : t.gb;
                     if (!args.a_mn) {
@@ -576,20 +597,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             tma_load_3d(base + C::OFF_A + s * C::A_BYTES + h * (BM * BK), &tm_a, fb,
                                         t.mb * C::TM + h * BM, kx, ga);
                     }
-                    if (args.b_mn) {
-                        // MN-major B (BN a multiple of 128): one box of 128 columns x 128 K per
-                        // 128 columns, 16 KB apart (the descriptor's leading-dimension stride)
+                    if (C::B_MN_OK && args.b_mn) {
+                        // MN-major B: one box of 128 columns x 128 K per 128 columns, 16 KB apart
+                        // (the descriptor's leading-dimension stride)
 #pragma unroll
-                        for (int j = 0; j < C::BN / 128; ++j)
-                            tma_load_3d(base + C::OFF_B + s * C::B_BYTES + j * (128 * BK), &tm_b, fb,
+                        for (int j = 0; j < C::B_BOXES; ++j)
+                            tma_load_3d(base + C::OFF_B + s * C::B_STAGE + j * (128 * BK), &tm_b, fb,
                                         t.nb * C::BN + j * 128, kx, gbz);
                     } else if (!pair) {
-                        tma_load_3d(base + C::OFF_B + s * C::B_BYTES, &tm_b, fb, kx, t.nb * C::BN, gbz);
+                        tma_load_3d(base + C::OFF_B + s * C::B_STAGE, &tm_b, fb, kx, t.nb * C::BN, gbz);
                     } else {
                         // The B map's box is half a tile; with multicast each CTA of the pair loads
                         // one half into both CTAs, otherwise each loads both halves itself.
                         constexpr int H = C::BN / 2;
-                        const uint32_t dst = base + C::OFF_B + s * C::B_BYTES;
+                        const uint32_t dst = base + C::OFF_B + s * C::B_STAGE;
                         if (t.mc) {
                             tma_load_3d_multicast(dst + crank * (H * BK), &tm_b, fb, kb * BK,
                                                   t.nb * C::BN + static_cast<int>(crank) * H, t.gb, 0x3);
@@ -685,7 +706,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     tc_fence_after_sync();
                     if (active) {
                         const uint64_t adesc = adesc0 + static_cast<uint64_t>((s * C::A_BYTES) >> 4);
-                        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((s * C::B_BYTES) >> 4);
+                        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((s * C::B_STAGE) >> 4);
                         const uint32_t sf_id = static_cast<uint32_t>(kb & 3);
                         const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
 #pragma unroll
@@ -745,11 +766,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (++sf_slot == C::SF_SLOTS) sf_slot = 0;
             }
         }
-    } else if ((warp >= 2 && warp <= 5) || (MH == 2 && warp >= 8)) {
+    } else if ((warp >= 2 && warp <= 5) || ((MH == 2 || C::EPI_COLS == 2) && warp >= 8)) {
         // ------------------------------------------------------------------ epilogue
-        // Warps 2-5 write half 0 of each tile, warps 8-11 (MH = 2) half 1.
+        // Warps 2-5 write half 0 of each tile, warps 8-11 half 1 (MH = 2) or the second half of
+        // the columns (EPI_COLS = 2).
         const uint32_t q = warp & 3u;                 // the TMEM lane quadrant this warp may read
-        const int my_half = warp >= 8 ? 1 : 0;
+        const int my_half = (MH == 2 && warp >= 8) ? 1 : 0;
+        constexpr int NCH = (C::BN + 31) / 32;        // 32-column chunks of a tile row
+        const int my_cols = (C::EPI_COLS == 2 && warp >= 8) ? 1 : 0;
+        const int ch_lo = my_cols * NCH / C::EPI_COLS, ch_hi = (my_cols + 1) * NCH / C::EPI_COLS;
+        const bool use_c = args.out_f32 && args.c != nullptr;
         const int row_in_half = static_cast<int>(q * 32 + lane);
         const int N = args.N;
         int acc = 0;
@@ -881,9 +907,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const int row = row_of(h);
                     bool write, zero_row;
                     row_state(row, write, zero_row);
-                    if (write) store_zero_row(args, roff_of(row), n0, min(N, n0 + C::BN));
+                    if (write) store_zero_row(args, roff_of(row), n0 + 32 * ch_lo, min(N, n0 + 32 * ch_hi));
                 }
                 continue;
+            }
+            if (use_c && ((t.hmask >> my_half) & 1u)) {
+                // Ask L2 for this thread's C segment while the tile's main loop still runs.
+                const int row = row_of(my_half);
+                const int c0 = n0 + 32 * ch_lo, c1 = min(N, n0 + 32 * ch_hi);
+                if (row < m_valid && c1 > c0)
+                    prefetch_l2(args.c + roff_of(row) + c0, static_cast<uint32_t>(c1 - c0) * 4u);
             }
             if (!wait_or_abort(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
             tc_fence_after_sync();
@@ -897,13 +930,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const uint32_t t_row =
                     tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>((acc * MH + h) * C::BN);
 #pragma unroll 1
-                for (int c = 0; c < (C::BN + 31) / 32; ++c) {
+                for (int c = ch_lo; c < ch_hi; ++c) {
                     uint32_t r[32];
                     const bool half_chunk = (C::BN % 32 != 0) && (c == C::BN / 32);   // 16-column tail
+                    const int ncols = half_chunk ? 16 : 32;
                     if (half_chunk) tmem_ld_32x32b_x16(t_row + 32u * c, r);
                     else tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                    float4 cv[8];
+                    // C's loads go out before the wait for the TMEM load, so the two overlap
+                    if (use_c && write) load_c_chunk(args, row_off, n0 + 32 * c, N, ncols, cv);
                     tmem_wait_ld();
-                    if (write) store_row_chunk(args, row_off, n0 + 32 * c, N, r, half_chunk ? 16 : 32, zero_row);
+                    if (write) store_row_chunk(args, row_off, n0 + 32 * c, N, r, ncols, zero_row, use_c ? cv : nullptr);
                 }
             }
         epilogue_release:
