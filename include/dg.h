@@ -121,6 +121,29 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
                                           const int32_t* sfb, void* d, const int32_t* masked_m,
                                           int G, int max_m, int N, int K, void* stream);
 
+/*
+ * FP8 x FP4: E4M3 activations times E2M1 weights, BF16 out (README "News" 2026.04.16: FP8xFP4
+ * GEMM; the DeepGEMM-Ascend article's FP8xFP4 row: FP4 as the weight format halves its memory).
+ * Same arguments, layouts, scales and semantics as dg_fp8_gemm_nt and the two M-grouped calls,
+ * except that B holds E2M1 codes packed two per byte:
+ *   b   uint8 [N][K/2] (dense) or [G][N][K/2] (grouped): K element 2i of a row in the low
+ *       nibble of byte i, element 2i + 1 in the high nibble; E2M1 = sign, 2 exponent bits
+ *       (bias 1), 1 mantissa bit: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6
+ *   sfb packed UE8M0 words exactly as for the FP8 calls: one word per row of B and group of
+ *       four 1x128 K blocks (per-row scales, or 128x128 block scales broadcast by
+ *       dg_pack_sf_ue8m0 with gran_mn = 128)
+ * b must be 32-byte aligned.  The weights cross HBM at half the FP8 bytes; in shared memory
+ * and in the tensor cores they take the FP8 path's footprint and rate.
+ */
+dg_status dg_fp8_fp4_gemm_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, void* d, int M,
+                             int N, int K, void* stream);
+dg_status dg_m_grouped_fp8_fp4_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b,
+                                                  const int32_t* sfb, void* d, const int32_t* m_indices, int M_sum,
+                                                  int N, int K, int G, void* stream);
+dg_status dg_m_grouped_fp8_fp4_gemm_nt_masked(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                              void* d, const int32_t* masked_m, int G, int max_m, int N, int K,
+                                              void* stream);
+
 /* Storage layouts of the operands of dg_fp8_gemm (README "Interface / Notes": the SM100 kernels
  * take the NT, TN, NN and TT layouts).  The first letter is A's, the second B's:
  *   A 'n': [M, K], K contiguous        A 't': [K, M], M contiguous (MN-major)

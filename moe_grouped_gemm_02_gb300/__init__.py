@@ -28,7 +28,8 @@ EXPORTS = ("dg_fp8_gemm_nt", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_groupe
            "dg_pack_sf_ue8m0", "dg_get_mk_alignment_for_contiguous_layout", "dg_get_tma_aligned_size",
            "dg_set_num_sms", "dg_get_num_sms", "dg_set_pdl", "dg_get_pdl", "dg_status_string",
            "dg_check_device_error", "dg_quantize_fp8_1x128", "dg_fp8_gemm",
-           "dg_k_grouped_fp8_gemm_tn_contiguous", "dg_pack_sf_ue8m0_k_grouped")
+           "dg_k_grouped_fp8_gemm_tn_contiguous", "dg_pack_sf_ue8m0_k_grouped", "dg_fp8_fp4_gemm_nt",
+           "dg_m_grouped_fp8_fp4_gemm_nt_contiguous", "dg_m_grouped_fp8_fp4_gemm_nt_masked")
 
 LAYOUTS = {"nt": 0, "nn": 1, "tn": 2, "tt": 3}
 
@@ -59,9 +60,13 @@ def load_library() -> ctypes.CDLL:
     lib.dg_fp8_gemm.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]
     lib.dg_k_grouped_fp8_gemm_tn_contiguous.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     lib.dg_pack_sf_ue8m0_k_grouped.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+    lib.dg_fp8_fp4_gemm_nt.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
+    lib.dg_m_grouped_fp8_fp4_gemm_nt_contiguous.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
+    lib.dg_m_grouped_fp8_fp4_gemm_nt_masked.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
     for name in ("dg_fp8_gemm_nt", "dg_m_grouped_fp8_gemm_nt_contiguous", "dg_m_grouped_fp8_gemm_nt_masked",
                  "dg_pack_sf_ue8m0", "dg_check_device_error", "dg_quantize_fp8_1x128", "dg_fp8_gemm",
-                 "dg_k_grouped_fp8_gemm_tn_contiguous", "dg_pack_sf_ue8m0_k_grouped"):
+                 "dg_k_grouped_fp8_gemm_tn_contiguous", "dg_pack_sf_ue8m0_k_grouped", "dg_fp8_fp4_gemm_nt",
+                 "dg_m_grouped_fp8_fp4_gemm_nt_contiguous", "dg_m_grouped_fp8_fp4_gemm_nt_masked"):
         getattr(lib, name).restype = i32
     lib.dg_check_device_error.argtypes = [vp]
     lib.dg_get_mk_alignment_for_contiguous_layout.argtypes = []
@@ -176,6 +181,32 @@ def dg_pack_sf_ue8m0_k_grouped(sf, out, ks, mn: int, stream=None) -> None:
 def k_grouped_packed_sf_rows(ks) -> int:
     """Rows of a K-grouped packed scale tensor: sum over groups of ceil(ks[g] / 512)."""
     return int(sum((int(k) // 128 + 3) // 4 for k in ks))
+
+
+def dg_fp8_fp4_gemm_nt(a, sfa, b, sfb, d, stream=None) -> None:
+    """d[M, N] = a[M, K] (E4M3) @ b^T, b E2M1 packed [N, K/2] (element 2i in the low nibble)."""
+    M, K = a.shape
+    N = b.shape[0]
+    _check("dg_fp8_fp4_gemm_nt", load_library().dg_fp8_fp4_gemm_nt(
+        _ptr(a, "a"), _ptr(sfa, "sfa"), _ptr(b, "b"), _ptr(sfb, "sfb"), _ptr(d, "d"), M, N, K, _stream(stream)))
+
+
+def dg_m_grouped_fp8_fp4_gemm_nt_contiguous(a, sfa, b, sfb, d, m_indices, stream=None) -> None:
+    """The contiguous-layout grouped GEMM with E2M1 experts b [G, N, K/2]."""
+    M_sum, K = a.shape
+    G, N, _ = b.shape
+    _check("dg_m_grouped_fp8_fp4_gemm_nt_contiguous", load_library().dg_m_grouped_fp8_fp4_gemm_nt_contiguous(
+        _ptr(a, "a"), _ptr(sfa, "sfa"), _ptr(b, "b"), _ptr(sfb, "sfb"), _ptr(d, "d"),
+        _ptr(m_indices, "m_indices"), M_sum, N, K, G, _stream(stream)))
+
+
+def dg_m_grouped_fp8_fp4_gemm_nt_masked(a, sfa, b, sfb, d, masked_m, stream=None) -> None:
+    """The masked-layout grouped GEMM with E2M1 experts b [G, N, K/2]."""
+    G, max_m, K = a.shape
+    N = b.shape[1]
+    _check("dg_m_grouped_fp8_fp4_gemm_nt_masked", load_library().dg_m_grouped_fp8_fp4_gemm_nt_masked(
+        _ptr(a, "a"), _ptr(sfa, "sfa"), _ptr(b, "b"), _ptr(sfb, "sfb"), _ptr(d, "d"),
+        _ptr(masked_m, "masked_m"), G, max_m, N, K, _stream(stream)))
 
 
 def dg_m_grouped_fp8_gemm_nt_contiguous(a, sfa, b, sfb, d, m_indices, stream=None) -> None:

@@ -130,6 +130,20 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int al4(int x) { return (x + 3) / 4 * 4; }
 
+// 3-D tiled map; row_bytes is the pitch of dimension 1 (d0 elements, which for packed 4-bit
+// types is d0 / 2 bytes).
+bool encode_3d_pitch(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t d0, uint64_t d1,
+                     uint64_t d2, uint64_t row_bytes, uint32_t b0, uint32_t b1, CUtensorMapSwizzle swz) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {row_bytes, row_bytes * d1};
+    cuuint32_t box[3] = {b0, b1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, uint64_t elem_bytes, const void* ptr, uint64_t d0,
                uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1, CUtensorMapSwizzle swz) {
     auto fn = encode_fn();
@@ -168,7 +182,7 @@ int cluster_capacity(DeviceState& st, int cfg_index, const KernelConfig* c, int 
 }
 
 Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N, int kblocks, int sms,
-                 int extra_ints, int b_mn) {
+                 int extra_ints, int b_mn, int b_fp4) {
     int n = 0;
     const KernelConfig* const* cfgs = all_configs(&n);
     const int ngroups = (kblocks + 3) / 4;
@@ -192,7 +206,7 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                 if (pair && split > 1) continue;
                 // MN-major B is loaded in boxes of 128 columns; K-grouped tiles have per-group K.
                 if (b_mn && c->bn % 128 != 0 && c->mh != 2) continue;
-                if ((b_mn || mode == MODE_K_GROUPED) && pair) continue;
+                if ((b_mn || b_fp4 || mode == MODE_K_GROUPED) && pair) continue;
                 if (mode == MODE_K_GROUPED && split > 1) continue;
                 // one 128-row half with one accumulator: the epilogue warps split the columns,
                 // which the split-K reduction does not support
@@ -246,6 +260,7 @@ struct GemmCall {
     const float* c = nullptr;       // FP32 C (out_f32 only)
     int out_f32 = 0;
     int a_mn = 0, b_mn = 0;         // operand stored MN-major
+    int b_fp4 = 0;                  // B is E2M1, two per byte
     const int32_t* m_indices = nullptr;
     const int32_t* masked_m = nullptr;
     const int32_t* ks = nullptr;    // K-grouped: K rows per group
@@ -330,7 +345,8 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     // Kb / 4 + G rows in all (each group rounds its own count up).
     const int plan_kb = kgrouped ? std::max(1, (Kb + groups - 1) / groups) : Kb;
     const int kp_rows = kgrouped ? Kb / 4 + groups : Kp;
-    const Plan plan = choose_plan(*st, mode, rows, m_blocks * groups, N, plan_kb, sms, extra_ints, call.b_mn);
+    const Plan plan =
+        choose_plan(*st, mode, rows, m_blocks * groups, N, plan_kb, sms, extra_ints, call.b_mn, call.b_fp4);
     if (!plan.cfg) return DG_ERR_SHAPE;   // nothing fits in shared memory (too many groups)
     const KernelConfig* cfg = plan.cfg;
 
@@ -345,10 +361,17 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
                                     CU_TENSOR_MAP_SWIZZLE_128B)
                         : encode_3d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, Km, rows, a_groups, 128,
                                     128 * cfg->mh, CU_TENSOR_MAP_SWIZZLE_128B);
-    ok = ok && (call.b_mn ? encode_3d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, N, Km, bz, 128, 128,
-                                      CU_TENSOR_MAP_SWIZZLE_128B)
-                          : encode_3d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, Km, N, bz, 128,
-                                      plan.pair ? cfg->bn / 2 : cfg->bn, CU_TENSOR_MAP_SWIZZLE_128B));
+    if (call.b_fp4) {
+        // E2M1 B, K-major: the TMA unpacks each 8 bytes (16 values) into a 16-byte unit, so a
+        // 128-value box row fills a 128-byte swizzled row as an E4M3 row does.
+        ok = ok && encode_3d_pitch(&maps[1], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, b, Km, N, bz,
+                                   static_cast<uint64_t>(Km) / 2, 128, cfg->bn, CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+        ok = ok && (call.b_mn ? encode_3d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, N, Km, bz, 128, 128,
+                                          CU_TENSOR_MAP_SWIZZLE_128B)
+                              : encode_3d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, Km, N, bz, 128,
+                                          plan.pair ? cfg->bn / 2 : cfg->bn, CU_TENSOR_MAP_SWIZZLE_128B));
+    }
     ok = ok && encode_3d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfa, al4(rows), kp_rows, a_groups,
                          128 * cfg->mh, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
     ok = ok && encode_3d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfb, al4(N), kp_rows, bz, cfg->bn, 1,
@@ -371,6 +394,7 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     args.a_mn = call.a_mn;
     args.b_mn = call.b_mn;
     args.out_f32 = call.out_f32;
+    args.b_fp4 = call.b_fp4;
     args.c = call.c;
     args.d = call.d;
     args.err = st->err_ptr;
@@ -419,6 +443,11 @@ dg_status check_common(const void* a, const int32_t* sfa, const void* b, const i
     if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(d))
         return DG_ERR_ALIGNMENT;
     return DG_OK;
+}
+
+// E2M1 B needs a 32-byte aligned base for the unpacking TMA, on top of the common checks.
+dg_status check_fp4_b(const void* b) {
+    return (reinterpret_cast<uintptr_t>(b) & 31u) ? DG_ERR_ALIGNMENT : DG_OK;
 }
 
 }  // namespace
@@ -473,6 +502,62 @@ dg_status dg_m_grouped_fp8_gemm_nt_masked(const void* a, const int32_t* sfa, con
     GemmCall call;
     call.mode = MODE_MASKED;
     call.a = a, call.sfa = sfa, call.b = b, call.sfb = sfb, call.d = d;
+    call.masked_m = masked_m;
+    call.groups = G, call.b_groups = G, call.rows = max_m, call.N = N, call.K = K;
+    return run_gemm(call, stream);
+}
+
+dg_status dg_fp8_fp4_gemm_nt(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb, void* d, int M,
+                             int N, int K, void* stream) {
+    if (M < 0) return DG_ERR_INVALID_ARG;
+    dg_status s = check_common(a, sfa, b, sfb, d, N, K);
+    if (s != DG_OK) return s;
+    if ((s = check_fp4_b(b)) != DG_OK) return s;
+    if (static_cast<long long>(M) * K >= (1ll << 40) || static_cast<long long>(N) * K >= (1ll << 40))
+        return DG_ERR_SHAPE;
+    if (M == 0) return DG_OK;
+    GemmCall call;
+    call.a = a, call.sfa = sfa, call.b = b, call.sfb = sfb, call.d = d;
+    call.b_fp4 = 1;
+    call.rows = M, call.N = N, call.K = K;
+    return run_gemm(call, stream);
+}
+
+dg_status dg_m_grouped_fp8_fp4_gemm_nt_contiguous(const void* a, const int32_t* sfa, const void* b,
+                                                  const int32_t* sfb, void* d, const int32_t* m_indices, int M_sum,
+                                                  int N, int K, int G, void* stream) {
+    if (M_sum < 0 || G <= 0 || !m_indices) return DG_ERR_INVALID_ARG;
+    dg_status s = check_common(a, sfa, b, sfb, d, N, K);
+    if (s != DG_OK) return s;
+    if ((s = check_fp4_b(b)) != DG_OK) return s;
+    if (M_sum % 128 != 0) return DG_ERR_SHAPE;
+    if (static_cast<long long>(M_sum) * K >= (1ll << 40) || static_cast<long long>(G) * N * K >= (1ll << 40))
+        return DG_ERR_SHAPE;
+    if (M_sum == 0) return DG_OK;
+    GemmCall call;
+    call.mode = MODE_CONTIGUOUS;
+    call.a = a, call.sfa = sfa, call.b = b, call.sfb = sfb, call.d = d;
+    call.b_fp4 = 1;
+    call.m_indices = m_indices;
+    call.b_groups = G, call.rows = M_sum, call.N = N, call.K = K;
+    return run_gemm(call, stream);
+}
+
+dg_status dg_m_grouped_fp8_fp4_gemm_nt_masked(const void* a, const int32_t* sfa, const void* b, const int32_t* sfb,
+                                              void* d, const int32_t* masked_m, int G, int max_m, int N, int K,
+                                              void* stream) {
+    if (max_m < 0 || G <= 0 || !masked_m) return DG_ERR_INVALID_ARG;
+    if (G > kMaxMaskedGroups) return DG_ERR_SHAPE;
+    dg_status s = check_common(a, sfa, b, sfb, d, N, K);
+    if (s != DG_OK) return s;
+    if ((s = check_fp4_b(b)) != DG_OK) return s;
+    if (static_cast<long long>(G) * max_m * K >= (1ll << 40) || static_cast<long long>(G) * N * K >= (1ll << 40))
+        return DG_ERR_SHAPE;
+    if (max_m == 0) return DG_OK;
+    GemmCall call;
+    call.mode = MODE_MASKED;
+    call.a = a, call.sfa = sfa, call.b = b, call.sfb = sfb, call.d = d;
+    call.b_fp4 = 1;
     call.masked_m = masked_m;
     call.groups = G, call.b_groups = G, call.rows = max_m, call.N = N, call.K = K;
     return run_gemm(call, stream);

@@ -585,7 +585,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         continue;
                     }
                     const uint32_t fb = full_bar(s);
-                    mbar_arrive_expect_tx(fb, args.b_mn ? C::A_BYTES + C::B_BOXES * 128 * BK : C::TX_AB);
+                    // An unpacking E2M1 load counts the packed bytes it reads (half its shared-memory
+                    // footprint); an MN-major B arrives in whole 128-column boxes.
+                    mbar_arrive_expect_tx(fb, args.b_fp4  ? C::A_BYTES + C::B_BYTES / 2
+                                              : args.b_mn ? C::A_BYTES + C::B_BOXES * 128 * BK
+                                                          : C::TX_AB);
                     const int kx = (t.koff + kb) * BK;
                     const int gbz = args.mode == MODE_K_GROUPED ? 0 : t.gb;
                     if (!args.a_mn) {
@@ -664,7 +668,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                               : smem_desc_kmajor_sw128(base + C::OFF_B);
             const uint64_t astep = args.a_mn ? 256ull : 2ull;
             const uint64_t bstep = args.b_mn ? 256ull : 2ull;
-            const uint32_t idesc0 = idesc_mxf8_e4m3(BM, C::BN, 0) | idesc_mn_major(args.a_mn, args.b_mn);
+            const uint32_t idesc0 = idesc_mxf8_e4m3(BM, C::BN, 0) | idesc_mn_major(args.a_mn, args.b_mn) |
+                                    (args.b_fp4 ? idesc_b_e2m1() : 0u);
             for (int u = u_first; ok && u < total_units; u += u_step) {
                 const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
                 if (t.zero) continue;

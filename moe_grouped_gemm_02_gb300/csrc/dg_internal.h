@@ -32,6 +32,7 @@ struct GemmArgs {
     int a_mn;           // 1: A is stored MN-major ([K, rows], rows contiguous)
     int b_mn;           // 1: B is stored MN-major ([K, N], N contiguous)
     int out_f32;        // 1: D is FP32; 0: BF16
+    int b_fp4;          // 1: B is E2M1, unpacked by TMA into 16-byte units of 16 values
     const int32_t* m_indices;
     const int32_t* masked_m;
     const int32_t* ks;  // K-grouped: K rows of each group (multiples of 128)

@@ -343,6 +343,9 @@ __device__ __forceinline__ uint64_t smem_desc_sf_chunk(uint32_t saddr) {
 // Instruction descriptor for kind::mxf8f6f4 with E4M3 A and B, both K-major, UE8M0 scales,
 // FP32 accumulation: B scale byte id (bits 4-5), A/B formats (7-9, 10-12; E4M3 = 0),
 // N >> 3 (17-22), scale type UE8M0 (bit 23), M >> 4 (24-28), A scale byte id (29-30).
+// Instruction-descriptor B format field (bits 10-12) for E2M1 B operands.
+__host__ __device__ constexpr uint32_t idesc_b_e2m1() { return 5u << 10; }
+
 // Instruction-descriptor bits 15 and 16: A, respectively B, is MN-major in shared memory.
 __host__ __device__ constexpr uint32_t idesc_mn_major(int a_mn, int b_mn) {
     return (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);

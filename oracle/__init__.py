@@ -31,6 +31,8 @@ float64, so that it can be checked against the pages by eye:
     get_k_grouped_mn_major_tma_aligned_packed_ue8m0_tensor).
   * per-token 1x128 FP8 quantisation writing packed scales (README "Interface /
     Notes": quantisation is left to the caller, to be fused into a producer).
+  * FP8 x FP4: E4M3 activations times E2M1 weights (README "News" 2026.04.16;
+    the DeepGEMM-Ascend article's FP8xFP4 row and its note on FP4 weights).
 
 Readings where the pages are silent (each listed in the design notes):
   P2  byte j of packed word kp holds K block 4*kp + j (little-endian).
@@ -47,6 +49,10 @@ Readings where the pages are silent (each listed in the design notes):
   P14 K-grouped scales: one FP32 scale per 128-row K block and per column of the
       MN-major operand ([sum Kb][MN]), packed per group so that no packed word
       spans two groups; every ks[g] is a multiple of 128.
+  P15 FP4 weights: E2M1 codes packed two per byte, element 2i in the low nibble;
+      their scales are the same packed UE8M0 1x128 words as FP8 B's (one per row
+      and 128-wide K block) -- the pages fix neither the nibble order nor the
+      FP4 scale granularity.
   P1  (per-token quantisation) the scale of a 1x128 block is 2**e with e the smallest integer
       such that 448 * 2**e >= amax, clamped to [-127, 127], 0 for an all-zero block.
 """
@@ -56,4 +62,6 @@ from .reference import (  # noqa: F401
     fp8_gemm_nt, fp8_gemm_nt_unrounded, m_grouped_fp8_gemm_nt_contiguous,
     m_grouped_fp8_gemm_nt_masked, e4m3_encode_rne, block_scale_exponent, quantize_fp8_1x128,
     f32_round, fp8_gemm, k_group_offsets, pack_sf_ue8m0_k_grouped, k_grouped_fp8_gemm_tn_contiguous,
+    e2m1_decode_table, fp4_unpack, fp8_fp4_gemm_nt_unrounded, fp8_fp4_gemm_nt,
+    m_grouped_fp8_fp4_gemm_nt_contiguous, m_grouped_fp8_fp4_gemm_nt_masked,
 )

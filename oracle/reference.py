@@ -413,3 +413,104 @@ def k_grouped_fp8_gemm_tn_contiguous(a_codes, sfa_packed, b_codes, sfb_packed, k
             d = d + np.asarray(c[g], dtype=np.float32).astype(np.float64)
         out[g] = f32_round(d)
     return out
+
+
+# ---------------------------------------------------------------------------
+# FP8 x FP4 (README "News" 2026.04.16: FP8xFP4 GEMM; the DeepGEMM-Ascend article: FP4 as the
+# weight format, mixed with FP8 activations)
+# ---------------------------------------------------------------------------
+
+def _e2m1_value(code: int) -> float:
+    """The 4-bit E2M1 value of one code: sign, 2 exponent bits (bias 1), 1 mantissa bit.
+
+    Exponent field 0 is subnormal, (m/2) * 2**0; otherwise (1 + m/2) * 2**(e - 1).  Every
+    code is finite: the magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4 and 6.
+    """
+    s = (code >> 3) & 1
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    mag = (m / 2.0) if e == 0 else (1.0 + m / 2.0) * 2.0 ** (e - 1)
+    return -mag if s else mag
+
+
+_E2M1 = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def e2m1_decode_table() -> np.ndarray:
+    """float64[16]: the value of every E2M1 code."""
+    return _E2M1.copy()
+
+
+def fp4_unpack(packed: np.ndarray) -> np.ndarray:
+    """uint8 [..., K/2] -> E2M1 codes uint8 [..., K]: element 2i is the low nibble of byte i,
+    element 2i + 1 the high nibble."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def _fp4_block_products(a_codes, b_codes4, kb):
+    """sum_{k in block kb} e4m3(A[m,k]) * e2m1(B[n,k]), exactly: the products are multiples of
+    2**-10 below 2688, so 128-term sums need fewer than 32 bits and float64 holds them in any
+    order."""
+    ks = slice(kb * BLOCK_K, (kb + 1) * BLOCK_K)
+    return e4m3_decode(a_codes[:, ks]) @ _E2M1[b_codes4[:, ks]].T
+
+
+def fp8_fp4_gemm_nt_unrounded(a_codes, sfa_packed, b_packed, sfb_packed) -> np.ndarray:
+    """float64 D = A @ B^T with A E4M3 [M, K] and B E2M1 packed two per byte [N, K/2]; scales as
+    for fp8_gemm_nt_unrounded (packed UE8M0, one word per row, 1x128 K blocks)."""
+    a_codes = np.asarray(a_codes, dtype=np.uint8)
+    b4 = fp4_unpack(b_packed)
+    M, K = a_codes.shape
+    N = b4.shape[0]
+    assert K % BLOCK_K == 0 and b4.shape[1] == K
+    Kb = K // BLOCK_K
+    sa = unpack_sf_ue8m0(sfa_packed, M, Kb)[0]
+    sb = unpack_sf_ue8m0(sfb_packed, N, Kb)[0]
+    d = np.zeros((M, N), dtype=np.float64)
+    for kb in range(Kb):
+        scale = ue8m0_decode(sa[:, kb])[:, None] * ue8m0_decode(sb[:, kb])[None, :]
+        d += scale * _fp4_block_products(a_codes, b4, kb)
+    return d
+
+
+def fp8_fp4_gemm_nt(a_codes, sfa_packed, b_packed, sfb_packed) -> np.ndarray:
+    """BF16 bits [M, N] of D = A @ B^T, FP8 A and FP4 B, rounded once."""
+    return bf16_round_bits(fp8_fp4_gemm_nt_unrounded(a_codes, sfa_packed, b_packed, sfb_packed))
+
+
+def m_grouped_fp8_fp4_gemm_nt_contiguous(a_codes, sfa_packed, b_packed, sfb_packed, m_indices, rows=None):
+    """The contiguous-layout grouped GEMM with FP4 experts b_packed [G, N, K/2]: row m with
+    e = m_indices[m] >= 0 is A[m] @ B[e]^T, rows with -1 are +0.0."""
+    a_codes = np.asarray(a_codes, dtype=np.uint8)
+    m_indices = np.asarray(m_indices, dtype=np.int64)
+    M_sum, K = a_codes.shape
+    G, N, _ = b_packed.shape
+    Kb = K // BLOCK_K
+    rows = np.arange(M_sum) if rows is None else np.asarray(rows, dtype=np.int64)
+    sa_all = unpack_sf_ue8m0(sfa_packed, M_sum, Kb)[0]
+    out = np.zeros((rows.size, N), dtype=np.uint16)
+    for e in range(G):
+        sel = np.nonzero(m_indices[rows] == e)[0]
+        if sel.size:
+            r = rows[sel]
+            out[sel] = fp8_fp4_gemm_nt(a_codes[r], _repack_rows(sa_all[r]), b_packed[e], sfb_packed[e])
+    return out
+
+
+def m_grouped_fp8_fp4_gemm_nt_masked(a_codes, sfa_packed, b_packed, sfb_packed, masked_m, d_prior):
+    """The masked-layout grouped GEMM with FP4 experts: rows m < masked_m[g] of group g are
+    A[g][m] @ B[g]^T, every other row keeps d_prior's bits."""
+    a_codes = np.asarray(a_codes, dtype=np.uint8)
+    G, max_m, K = a_codes.shape
+    out = np.array(d_prior, dtype=np.uint16, copy=True)
+    Kb = K // BLOCK_K
+    for g in range(G):
+        m = int(masked_m[g])
+        if m > 0:
+            sa = unpack_sf_ue8m0(sfa_packed[g], max_m, Kb)[0][:m]
+            out[g, :m] = fp8_fp4_gemm_nt(a_codes[g, :m], _repack_rows(sa), b_packed[g], sfb_packed[g])
+    return out

@@ -211,6 +211,40 @@ def make_k_grouped(M: int, N: int, ks, seed: int = 0, a_outliers: bool = True) -
                 b=np.ascontiguousarray(b_q.T), sfb=np.ascontiguousarray(b_sf.T))
 
 
+_E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def quantize_fp4_1x128(x: np.ndarray):
+    """Per-row 1x128 block quantisation of x[..., R, K] to E2M1, packed two per byte (element
+    2i in the low nibble).  Scale 2**e with e the smallest integer such that 6 * 2**e >= amax
+    (0 for an all-zero block); codes round x / 2**e to the nearest E2M1 value, ties to the
+    code with an even mantissa bit.  Returns (packed uint8 [..., R, K/2], sf float32 [..., R, K/128])."""
+    *lead, R, K = x.shape
+    xb = np.asarray(x, dtype=np.float64).reshape(*lead, R, K // BLOCK, BLOCK)
+    amax = np.abs(xb).max(axis=-1)
+    f, fe = np.frexp(amax)                      # amax = f * 2**fe, f in [0.5, 1)
+    e = fe.astype(np.int64) - 3 + (f > 0.75)    # 6 * 2**(fe-3) = 0.75 * 2**fe
+    e = np.where(amax == 0, 0, np.clip(e, -127, 127))
+    y = np.abs(xb) / np.ldexp(1.0, e)[..., None]
+    hi = np.minimum(np.searchsorted(_E2M1_GRID, y, side="left"), 7)
+    lo = np.maximum(hi - 1, 0)
+    d_hi, d_lo = _E2M1_GRID[hi] - y, y - _E2M1_GRID[lo]
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0)) | (d_hi == 0)
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(np.signbit(xb) & (code > 0), code | 8, code).reshape(*lead, R, K).astype(np.uint8)
+    packed = (code[..., 0::2] | (code[..., 1::2] << 4)).astype(np.uint8)
+    return packed, np.ldexp(np.float32(1.0), e).astype(np.float32)
+
+
+def with_fp4_b(w: dict, seed: int, b_std: float = 0.02) -> dict:
+    """The same workload with FP4 weights: B [..., N, K] redrawn (same stream) and quantized
+    to E2M1 with per-row 1x128 scales (sfb [..., N, K/128]); b_fp4 holds the packed bytes."""
+    shape = w["b"].shape
+    b = normal(shape, seed, "b", std=b_std)
+    packed, sf = quantize_fp4_1x128(b)
+    return dict(w, b_fp4=packed, sfb_fp4=sf)
+
+
 SENTINEL_BF16 = 0x7FA5   # a NaN pattern used to pre-fill D where rows must stay untouched
 
 

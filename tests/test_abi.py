@@ -88,3 +88,15 @@ def test_quantize_validation(lib):
     assert f(GOOD, GOOD, GOOD, 1, 64, 1000, None) == 2        # K % 128
     assert f(GOOD, GOOD, ODD, 1, 64, 1024, None) == 3         # misaligned scales
     assert f(GOOD, GOOD, GOOD, 1, 0, 1024, None) == 0         # empty: no-op
+
+
+def test_fp4_validation(lib):
+    f = lib.dg_fp8_fp4_gemm_nt
+    ODD16 = P(0x10010)       # 16-byte but not 32-byte aligned
+    assert f(GOOD, GOOD, ODD16, GOOD, GOOD, 128, 512, 1024, None) == 3
+    assert f(GOOD, GOOD, GOOD, GOOD, GOOD, 128, 512, 1000, None) == 2
+    assert f(GOOD, GOOD, GOOD, GOOD, GOOD, 0, 512, 1024, None) == 0
+    c = lib.dg_m_grouped_fp8_fp4_gemm_nt_contiguous
+    assert c(GOOD, GOOD, ODD16, GOOD, GOOD, GOOD, 256, 512, 1024, 4, None) == 3
+    m = lib.dg_m_grouped_fp8_fp4_gemm_nt_masked
+    assert m(GOOD, GOOD, GOOD, GOOD, GOOD, None, 4, 256, 512, 1024, None) == 1

@@ -564,3 +564,44 @@ def test_k_grouped_gemm_brute_force():
     no_c = oracle.k_grouped_fp8_gemm_tn_contiguous(a, oracle.pack_sf_ue8m0_k_grouped(sa, M, ks), b,
                                                    oracle.pack_sf_ue8m0_k_grouped(sb, N, ks), ks)
     assert np.all(no_c[1] == 0) and no_c[1].tobytes() == np.zeros((M, N), np.float32).tobytes()
+
+
+# ---------------------------------------------------------------------------
+# FP8 x FP4
+# ---------------------------------------------------------------------------
+
+def test_e2m1_table_is_the_format():
+    # E2M1 (the 4-bit MX element format): magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; bit 3 the sign
+    t = oracle.e2m1_decode_table()
+    assert list(t[:8]) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert np.array_equal(t[8:], -t[:8]) and np.signbit(t[8])
+    # every value times 2 is an integer and the spacing doubles per binade
+    assert np.all((t[:8] * 2) == np.round(t[:8] * 2))
+
+
+def test_fp4_unpack_nibble_order():
+    p = np.array([[0x21, 0xF0]], np.uint8)
+    assert oracle.fp4_unpack(p).tolist() == [[1, 2, 0, 15]]
+
+
+def test_fp8_fp4_gemm_brute_force():
+    rs = np.random.default_rng(41)
+    M, N, K = 3, 4, 256
+    a = _finite_codes(rs, (M, K))
+    b4 = rs.integers(0, 16, size=(N, K)).astype(np.uint8)
+    packed = (b4[:, 0::2] | (b4[:, 1::2] << 4)).astype(np.uint8)
+    sa = np.ldexp(np.float32(1), rs.integers(-6, 7, (M, 2))).astype(np.float32)
+    sb = np.ldexp(np.float32(1), rs.integers(-6, 7, (N, 2))).astype(np.float32)
+    got = oracle.fp8_fp4_gemm_nt_unrounded(a, oracle.pack_sf_ue8m0(sa, M, 1)[0], packed,
+                                           oracle.pack_sf_ue8m0(sb, N, 1)[0])
+    av = _dec(a)
+    # E2M1 by its definition, one code at a time
+    def e2m1(c):
+        s, e, m = c >> 3, (c >> 1) & 3, c & 1
+        v = m * 0.5 if e == 0 else (1 + m * 0.5) * 2.0 ** (e - 1)
+        return -v if s else v
+    for m in range(M):
+        for n in range(N):
+            terms = [av[m, k] * e2m1(int(b4[n, k])) * float(sa[m, k // 128]) * float(sb[n, k // 128])
+                     for k in range(K)]
+            assert got[m, n] == math.fsum(terms)
