@@ -438,40 +438,152 @@ NEXT_QUANTIZE = [("quantize_32768x7168_bf16", 32768, 7168),     # the contiguous
                  ("quantize_4096x16384_bf16", 4096, 16384)]     # the prefill A
 
 
+# The K-grouped weight-gradient GEMM of the contiguous MoE layer: dW_e = dY_e^T X_e for 4
+# experts, M = 4096 (the layer's N), N = 7168 (its K), the experts' token counts (the same
+# multinomial draw as the forward workload) padded to multiples of 128, FP32 accumulation
+# into the gradients in place.
+NEXT_K_GROUPED = ("k_grouped_wgrad_4x4096x7168_32768tok_f32acc", 4096, 7168)
+# The prefill shape in the NN layout (B stored [K, N]) with FP32 output accumulated in place.
+NEXT_LAYOUT = ("prefill_nn_f32acc_4096x7168x16384", 4096, 7168, 16384)
+
+
+def _time_launches(fn, stream, flush, reps):
+    """Median, min and max ms of `reps` launches of fn: CUDA events on the launching stream,
+    L2 flushed (256 MB written) before every rep."""
+    ts = []
+    for r in range(reps):
+        flush.fill_(float(r))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts), min(ts), max(ts)
+
+
+def _random_e4m3(shape, gen, dev):
+    """N(0, 1) values as E4M3 codes (timing inputs: the tensor cores' speed does not depend on them)."""
+    return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
 def time_next_rows(dev, peaks, reps: int = 20):
-    """Per-token 1x128 FP8 quantisation: ms per launch (median of `reps`, CUDA events on the
-    launching stream, L2 flushed before every rep), algorithmic bytes = 2 MK read + MK codes
-    + 4 Kp al4(M) scale bytes written."""
+    """Kernels timed beside the GEMM step, each alone on its own workload, L2 flushed before every
+    rep: the per-token quantisation (algorithmic bytes = 2 MK read + MK codes + 4 Kp al4(M)
+    scale bytes written), the K-grouped weight-gradient GEMM and the NN-layout FP32-accumulating
+    GEMM (2 M N K flops each)."""
     import moe_grouped_gemm_02_gb300 as dg
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)     # 256 MB > L2
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
+    fp8_peak = peaks["bf16"] * FP8_OVER_BF16
     rows = []
+
+    def hbm_row(row, name, ms, lo, hi, nbytes):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"row": row, "workload": name, "ms": round(ms, 5), "ms_min": round(lo, 5), "ms_max": round(hi, 5),
+                "bytes": nbytes, "gbs": round(gbs, 1), "bound": "hbm", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                "peak_source": f"hbm copy (of {peaks['source']})"}
+
+    def tensor_row(row, name, ms, lo, hi, flops, nbytes):
+        tf = flops / (ms * 1e-3) / 1e12
+        return {"row": row, "workload": name, "ms": round(ms, 5), "ms_min": round(lo, 5), "ms_max": round(hi, 5),
+                "flops": flops, "bytes": nbytes, "tflops": round(tf, 1), "bound": "tensor",
+                "frac": round(tf / fp8_peak, 4),
+                "peak_source": f"burst bf16 x {FP8_OVER_BF16:g} (of {peaks['source']})"}
+
     for name, M, K in NEXT_QUANTIZE:
         x = torch.randn((M, K), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
         q = torch.empty((M, K), dtype=torch.uint8, device=dev)
         sf = torch.empty(dg.packed_sf_shape(None, M, K), dtype=torch.int32, device=dev)
         for _ in range(3):
             dg.dg_quantize_fp8_1x128(x, q, sf)
-        ts = []
-        for r in range(reps):
-            flush.fill_(float(r))
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            dg.dg_quantize_fp8_1x128(x, q, sf)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
+        ms, lo, hi = _time_launches(lambda: dg.dg_quantize_fp8_1x128(x, q, sf), stream, flush, reps)
         dg.dg_check_device_error()
-        ms = statistics.median(ts)
-        nbytes = 3 * M * K + 4 * sf.numel()
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        rows.append({"row": "per-token 1x128 FP8 quantisation (dg_quantize_fp8_1x128)", "workload": name,
-                     "ms": round(ms, 5), "ms_min": round(min(ts), 5), "ms_max": round(max(ts), 5),
-                     "bytes": nbytes, "gbs": round(gbs, 1), "bound": "hbm",
-                     "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": f"hbm copy (of {peaks['source']})"})
+        rows.append(hbm_row("per-token 1x128 FP8 quantisation (dg_quantize_fp8_1x128)", name, ms, lo, hi,
+                            3 * M * K + 4 * sf.numel()))
         del x, q, sf
+
+    # K-grouped weight gradient
+    name, M, N = NEXT_K_GROUPED
+    counts = synth.rng(0, "counts").multinomial(synth.CONTIGUOUS["tokens"], [0.25] * 4)
+    ks = [synth.align_up(int(c), 128) for c in counts]
+    sum_k = sum(ks)
+    a = _random_e4m3((sum_k, M), gen, dev)
+    b = _random_e4m3((sum_k, N), gen, dev)
+    rows_sf = dg.k_grouped_packed_sf_rows(ks)
+    sfa = torch.full((rows_sf, dg.dg_get_tma_aligned_size(M)), 0x7F7F7F7F, dtype=torch.int32, device=dev)
+    sfb = torch.full((rows_sf, dg.dg_get_tma_aligned_size(N)), 0x7F7F7F7F, dtype=torch.int32, device=dev)
+    d = torch.zeros((4, M, N), dtype=torch.float32, device=dev)
+    ks_d = torch.tensor(ks, dtype=torch.int32, device=dev)
+    call = lambda: dg.dg_k_grouped_fp8_gemm_tn_contiguous(a, sfa, b, sfb, d, ks_d, c=d)
+    for _ in range(3):
+        call()
+    ms, lo, hi = _time_launches(call, stream, flush, reps)
+    dg.dg_check_device_error()
+    rows.append(tensor_row("K-grouped FP8 weight-gradient GEMM (dg_k_grouped_fp8_gemm_tn_contiguous), "
+                           "D += A^T B in place", name, ms, lo, hi, 2.0 * M * N * sum_k,
+                           sum_k * (M + N) + 2 * 4 * 4 * M * N))
+    del a, b, sfa, sfb, d
+
+    # NN layout, FP32 out accumulated in place
+    name, M, N, K = NEXT_LAYOUT
+    a = _random_e4m3((M, K), gen, dev)
+    b = _random_e4m3((K, N), gen, dev)
+    sfa = torch.full(dg.packed_sf_shape(None, M, K), 0x7F7F7F7F, dtype=torch.int32, device=dev)
+    sfb = torch.full(dg.packed_sf_shape(None, N, K), 0x7F7F7F7F, dtype=torch.int32, device=dev)
+    d = torch.zeros((M, N), dtype=torch.float32, device=dev)
+    call = lambda: dg.dg_fp8_gemm(a, sfa, b, sfb, d, layout="nn", c=d)
+    for _ in range(3):
+        call()
+    ms, lo, hi = _time_launches(call, stream, flush, reps)
+    dg.dg_check_device_error()
+    rows.append(tensor_row("FP8 GEMM, NN layout, D += A B^T in FP32 (dg_fp8_gemm)", name, ms, lo, hi,
+                           2.0 * M * N * K, M * K + N * K + 2 * 4 * M * N))
+    del a, b, sfa, sfb, d
+
+    # FP8 x FP4: the decode shapes and the masked MoE shape with E2M1 weights (HBM-bound: the
+    # weights are read once at half the FP8 bytes), and the prefill shape (tensor-bound)
+    def fp4_weights(shape):
+        return torch.randint(0, 256, shape, generator=gen, device=dev, dtype=torch.int32).to(torch.uint8)
+
+    for (M, N, K) in synth.DECODE_SHAPES + [synth.PREFILL_SHAPE]:
+        a = _random_e4m3((M, K), gen, dev)
+        b = fp4_weights((N, K // 2))
+        sfa = torch.full(dg.packed_sf_shape(None, M, K), 0x7F7F7F7F, dtype=torch.int32, device=dev)
+        sfb = torch.full(dg.packed_sf_shape(None, N, K), 0x7F7F7F7F, dtype=torch.int32, device=dev)
+        d = torch.empty((M, N), dtype=torch.int16, device=dev)
+        call = lambda: dg.dg_fp8_fp4_gemm_nt(a, sfa, b, sfb, d)
+        for _ in range(3):
+            call()
+        ms, lo, hi = _time_launches(call, stream, flush, reps)
+        dg.dg_check_device_error()
+        name = f"fp8xfp4_{'prefill' if M == 4096 else 'decode'}_{M}x{N}x{K}"
+        nbytes = M * K + N * K // 2 + 2 * M * N + 4 * (sfa.numel() + sfb.numel())
+        row = "FP8 x FP4 GEMM (dg_fp8_fp4_gemm_nt)"
+        if M == 4096:
+            rows.append(tensor_row(row, name, ms, lo, hi, 2.0 * M * N * K, nbytes))
+        else:
+            rows.append(hbm_row(row, name, ms, lo, hi, nbytes))
+        del a, b, sfa, sfb, d
+    G, max_m, N, K = (synth.MASKED[k] for k in ("G", "max_m", "N", "K"))
+    masked_m = synth.rng(0, "masked_m").integers(1, max_m + 1, size=G)
+    a = _random_e4m3((G, max_m, K), gen, dev)
+    b = fp4_weights((G, N, K // 2))
+    sfa = torch.full(dg.packed_sf_shape(G, max_m, K), 0x7F7F7F7F, dtype=torch.int32, device=dev)
+    sfb = torch.full(dg.packed_sf_shape(G, N, K), 0x7F7F7F7F, dtype=torch.int32, device=dev)
+    d = torch.empty((G, max_m, N), dtype=torch.int16, device=dev)
+    mm = torch.tensor(masked_m, dtype=torch.int32, device=dev)
+    call = lambda: dg.dg_m_grouped_fp8_fp4_gemm_nt_masked(a, sfa, b, sfb, d, mm)
+    for _ in range(3):
+        call()
+    ms, lo, hi = _time_launches(call, stream, flush, reps)
+    dg.dg_check_device_error()
+    valid = int(masked_m.sum())
+    nbytes = valid * K + G * N * K // 2 + 2 * valid * N + 4 * (sfa.numel() + sfb.numel())
+    rows.append(hbm_row("FP8 x FP4 masked grouped GEMM (dg_m_grouped_fp8_fp4_gemm_nt_masked)",
+                        f"fp8xfp4_masked_{G}x{max_m}x{N}x{K}", ms, lo, hi, nbytes))
     return rows
 
 

@@ -168,6 +168,7 @@ struct Plan {
     int split = 1;
     int pair = 0;
     int capacity = 0;   // co-resident CTAs (plain) or clusters (split > 1, pair)
+    int tma_store = 0;  // room for the epilogue's output staging buffers
 };
 
 int cluster_capacity(DeviceState& st, int cfg_index, const KernelConfig* c, int cluster, int slot, int split,
@@ -175,7 +176,7 @@ int cluster_capacity(DeviceState& st, int cfg_index, const KernelConfig* c, int 
     std::lock_guard<std::mutex> lk(g_mu);
     int& v = st.clusters[cfg_index][slot];
     if (v == 0) {
-        v = c->max_clusters(cluster, c->smem_bytes(extra_ints, split));
+        v = c->max_clusters(cluster, c->smem_bytes(extra_ints, split, split > 1 ? 0 : 1));
         if (v <= 0) v = -1;
     }
     return v;
@@ -216,7 +217,8 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                 // would mostly compute padding unless the groups are deep.
                 if (c->mh > 1 && mode == MODE_MASKED && rows < 512 && !force_cfg) continue;
                 if (split > 1 && (ngroups < split || c->bn % 32 != 0)) continue;
-                if (c->smem_bytes(extra_ints, split) > static_cast<size_t>(st.max_smem)) continue;
+                if (c->smem_bytes(extra_ints, split, 0) > static_cast<size_t>(st.max_smem)) continue;
+                const int tma_store = split == 1 && c->smem_bytes(extra_ints, 1, 1) <= static_cast<size_t>(st.max_smem);
                 int cap = sms;
                 if (split > 1)
                     cap = std::min(cluster_capacity(st, i, c, split, split == 2 ? 0 : (split == 4 ? 1 : 2), split,
@@ -241,6 +243,7 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                     best.split = split;
                     best.pair = pair;
                     best.capacity = cap;
+                    best.tma_store = tma_store;
                     best_cost = cost;
                 }
             }
@@ -350,7 +353,7 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     if (!plan.cfg) return DG_ERR_SHAPE;   // nothing fits in shared memory (too many groups)
     const KernelConfig* cfg = plan.cfg;
 
-    CUtensorMap maps[4];
+    CUtensorMap maps[5];
     // A and D have one group per masked group; B one per expert (contiguous, masked).  K-grouped
     // operands are single [sum K, MN] matrices whose groups are K ranges.
     const int a_groups = mode == MODE_MASKED ? groups : 1;
@@ -376,6 +379,15 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
                          128 * cfg->mh, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
     ok = ok && encode_3d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfb, al4(N), kp_rows, bz, cfg->bn, 1,
                          CU_TENSOR_MAP_SWIZZLE_NONE);
+    // D, for the epilogue's bulk stores: boxes of 32 rows x 32 bytes (16 BF16 or 8 FP32 values).
+    const int d_groups = (mode == MODE_MASKED || kgrouped) ? groups : 1;
+    if (plan.tma_store)
+        ok = ok && (call.out_f32 ? encode_3d(&maps[4], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, call.d, N, rows, d_groups, 8,
+                                             32, CU_TENSOR_MAP_SWIZZLE_NONE)
+                                 : encode_3d(&maps[4], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, call.d, N, rows, d_groups,
+                                             16, 32, CU_TENSOR_MAP_SWIZZLE_NONE));
+    else
+        maps[4] = maps[0];   // unused
     if (!ok) return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
 
     GemmArgs args{};
@@ -407,6 +419,7 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     }
     args.debug_drop_stage = -1;
     args.pdl = pdl_enabled();
+    args.tma_store = plan.tma_store;
     if (const char* t = std::getenv("DG_DEBUG_DROP_LOAD")) args.debug_drop_stage = std::atoi(t);
     args.pair = plan.pair;
     args.num_m_units = (plan.pair || cfg->mh == 2) ? (m_blocks + 1) / 2 : m_blocks;

@@ -104,8 +104,16 @@ struct GemmCfg {
     static __host__ __device__ uint32_t recv_bytes(int split) {
         return split > 1 ? static_cast<uint32_t>((split - 1) * (BM / split) * RECV_ROW) : 0u;
     }
-    static size_t smem_bytes(int extra_ints, int split) {
-        return 1024 + off_recv(extra_ints) + recv_bytes(split);
+    // Without split-K the space after the prefix sums stages the epilogue's output boxes: two
+    // 1 KB buffers per epilogue warp (32 rows x 32 bytes each), the source of TMA bulk stores,
+    // which need 128-byte aligned shared-memory addresses (1024 here).
+    static constexpr uint32_t STAGE_OUT_BYTES = (EPI_THREADS / 32) * 2048;
+    static __host__ __device__ uint32_t off_stage_out(int extra_ints) {
+        return (static_cast<uint32_t>(OFF_CUM + extra_ints * 4) + 1023u) & ~1023u;
+    }
+    static size_t smem_bytes(int extra_ints, int split, int tma_store) {
+        if (split > 1) return 1024 + off_recv(extra_ints) + recv_bytes(split);
+        return 1024 + (tma_store ? off_stage_out(extra_ints) + STAGE_OUT_BYTES : off_recv(extra_ints));
     }
 };
 
@@ -384,7 +392,7 @@ template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
-                    const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tm_d, const GemmArgs args) {
     constexpr int MH = C::MH;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -407,7 +415,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const uint32_t redempty_bar = base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + 4);
     const int split = (MH == 1 && C::EPI_COLS == 1) ? args.split : 1;
     const int pair = MH == 1 ? args.pair : 0;
-    const uint32_t recv_base = base + C::off_recv(args.mode == MODE_MASKED ? args.groups + 1 : 0);
+    const uint32_t recv_base = base + C::off_recv(extra_smem_ints(args.mode, args.groups));
 
     if (threadIdx.x == 0) {
         // Arrivals per phase: a stage is released by every MMA issuer (and, in pair mode, by
@@ -433,6 +441,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         fence_mbarrier_init();
     }
     if (warp == 0 && lane == 0) {
+        if (args.tma_store) tma_prefetch_desc(&tm_d);
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
         tma_prefetch_desc(&tm_sfa);
@@ -781,6 +790,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int my_cols = (C::EPI_COLS == 2 && warp >= 8) ? 1 : 0;
         const int ch_lo = my_cols * NCH / C::EPI_COLS, ch_hi = (my_cols + 1) * NCH / C::EPI_COLS;
         const bool use_c = args.out_f32 && args.c != nullptr;
+        // This warp's two 1 KB output staging buffers (no split-K: the receive region is free).
+        const uint32_t ew = warp <= 5 ? warp - 2u : warp - 4u;     // epilogue warp index 0..7
+        const uint32_t stage_out = base + C::off_stage_out(extra_smem_ints(args.mode, args.groups)) + ew * 2048u;
+        uint32_t nbox = 0;                                          // boxes this warp has stored
         const int row_in_half = static_cast<int>(q * 32 + lane);
         const int N = args.N;
         int acc = 0;
@@ -934,6 +947,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const size_t row_off = roff_of(row);
                 const uint32_t t_row =
                     tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>((acc * MH + h) * C::BN);
+                // The warp's 32 rows go out as TMA boxes unless some of them must stay untouched
+                // (masked mode past masked_m[g]); rows past D's extent are clipped by the map.
+                const int slab0 = row - static_cast<int>(lane);
+                const bool slab_tma =
+                    args.tma_store && (args.mode != MODE_MASKED || slab0 + 32 <= m_valid) && slab0 < m_valid;
 #pragma unroll 1
                 for (int c = ch_lo; c < ch_hi; ++c) {
                     uint32_t r[32];
@@ -945,7 +963,70 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     // C's loads go out before the wait for the TMEM load, so the two overlap
                     if (use_c && write) load_c_chunk(args, row_off, n0 + 32 * c, N, ncols, cv);
                     tmem_wait_ld();
-                    if (write) store_row_chunk(args, row_off, n0 + 32 * c, N, r, ncols, zero_row, use_c ? cv : nullptr);
+                    if (!slab_tma) {
+                        if (write) store_row_chunk(args, row_off, n0 + 32 * c, N, r, ncols, zero_row, use_c ? cv : nullptr);
+                        continue;
+                    }
+                    // One box = 32 rows x 32 bytes: 16 BF16 or 8 FP32 columns (fully unrolled so
+                    // that r and cv stay in registers).
+                    auto put_box = [&](int col, uint4 w0, uint4 w1) {
+                        const uint32_t buf = stage_out + (nbox & 1u) * 1024u;
+                        if (nbox >= 2) {
+                            // the store that last read this buffer must be done reading it
+                            if (lane == 0) bulk_wait_group_read<1>();
+                            __syncwarp();
+                        }
+                        st_shared_v4(buf + lane * 32u, w0);
+                        st_shared_v4(buf + lane * 32u + 16u, w1);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&tm_d, buf, col, slab0, t.g);
+                            bulk_commit_group();
+                        }
+                        ++nbox;
+                    };
+                    const int col0 = n0 + 32 * c;
+                    if (args.out_f32) {
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            if (8 * b >= ncols) break;
+                            float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+                            if (!zero_row) {
+                                v0 = make_float4(__uint_as_float(r[8 * b]), __uint_as_float(r[8 * b + 1]),
+                                                 __uint_as_float(r[8 * b + 2]), __uint_as_float(r[8 * b + 3]));
+                                v1 = make_float4(__uint_as_float(r[8 * b + 4]), __uint_as_float(r[8 * b + 5]),
+                                                 __uint_as_float(r[8 * b + 6]), __uint_as_float(r[8 * b + 7]));
+                            }
+                            if (use_c && write) {
+                                v0.x += cv[2 * b].x, v0.y += cv[2 * b].y, v0.z += cv[2 * b].z, v0.w += cv[2 * b].w;
+                                v1.x += cv[2 * b + 1].x, v1.y += cv[2 * b + 1].y, v1.z += cv[2 * b + 1].z,
+                                    v1.w += cv[2 * b + 1].w;
+                            }
+                            put_box(col0 + 8 * b,
+                                    make_uint4(__float_as_uint(v0.x), __float_as_uint(v0.y), __float_as_uint(v0.z),
+                                               __float_as_uint(v0.w)),
+                                    make_uint4(__float_as_uint(v1.x), __float_as_uint(v1.y), __float_as_uint(v1.z),
+                                               __float_as_uint(v1.w)));
+                        }
+                    } else {
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            if (16 * b >= ncols) break;
+                            uint4 w0 = make_uint4(0, 0, 0, 0), w1 = w0;
+                            if (!zero_row) {
+                                w0 = make_uint4(pack_bf16x2(r[16 * b + 0], r[16 * b + 1]),
+                                                pack_bf16x2(r[16 * b + 2], r[16 * b + 3]),
+                                                pack_bf16x2(r[16 * b + 4], r[16 * b + 5]),
+                                                pack_bf16x2(r[16 * b + 6], r[16 * b + 7]));
+                                w1 = make_uint4(pack_bf16x2(r[16 * b + 8], r[16 * b + 9]),
+                                                pack_bf16x2(r[16 * b + 10], r[16 * b + 11]),
+                                                pack_bf16x2(r[16 * b + 12], r[16 * b + 13]),
+                                                pack_bf16x2(r[16 * b + 14], r[16 * b + 15]));
+                            }
+                            put_box(col0 + 16 * b, w0, w1);
+                        }
+                    }
                 }
             }
         epilogue_release:
@@ -953,6 +1034,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_arrive(tempty_bar(acc));
             if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
         }
+        if (lane == 0 && nbox > 0) bulk_wait_group_all();   // D is written before the CTA ends
+        __syncwarp();
     }
 
     tc_fence_before_sync();
@@ -968,8 +1051,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
 template <class C>
 cudaError_t launch_fp8_gemm(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStream_t stream) {
-    const int extra = args.mode == MODE_MASKED ? args.groups + 1 : 0;
-    const size_t smem = C::smem_bytes(extra, args.split);
+    const int extra = extra_smem_ints(args.mode, args.groups);
+    const size_t smem = C::smem_bytes(extra, args.split, args.tma_store);
     const int cluster = args.split > 1 ? args.split : (args.pair ? 2 : 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -992,7 +1075,7 @@ cudaError_t launch_fp8_gemm(const CUtensorMap* maps, const GemmArgs& args, int g
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<C>, maps[0], maps[1], maps[2], maps[3], args);
+    return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<C>, maps[0], maps[1], maps[2], maps[3], maps[4], args);
 }
 
 template <class C>

@@ -42,8 +42,16 @@ struct GemmArgs {
     unsigned long long timeout_ns;
     int debug_drop_stage;   // test hook: the producer skips this stage's loads (-1: never)
     int pdl;                // launch with programmatic dependent launch
+    int tma_store;          // the epilogue writes D through its tensor map (else plain stores)
 };
 
+// Shared-memory ints after the barriers: the masked-mode m-unit prefix sums (G + 1) or the
+// K-grouped K-block and scale-row prefix sums (2 (G + 1)).
+__host__ __device__ inline int extra_smem_ints(int mode, int groups) {
+    return mode == MODE_MASKED ? groups + 1 : (mode == MODE_K_GROUPED ? 2 * (groups + 1) : 0);
+}
+
+// maps: A, B, scales of A, scales of B, D
 using GemmLaunchFn = cudaError_t (*)(const CUtensorMap* maps, const GemmArgs& args, int grid,
                                      cudaStream_t stream);
 
@@ -53,7 +61,7 @@ struct KernelConfig {
     int acc;            // TMEM accumulator buffers
     int mh;             // 128-row halves per tile (2: one B tile serves 256 rows)
     const char* name;
-    size_t (*smem_bytes)(int extra_ints, int split);
+    size_t (*smem_bytes)(int extra_ints, int split, int tma_store);
     GemmLaunchFn launch;
     cudaError_t (*prepare)(int max_smem);   // per-device one-time kernel attribute setup
     int (*max_clusters)(int split, size_t smem);   // co-resident clusters of `split` CTAs
