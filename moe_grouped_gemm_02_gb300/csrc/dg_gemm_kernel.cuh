@@ -952,6 +952,62 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const int slab0 = row - static_cast<int>(lane);
                 const bool slab_tma =
                     args.tma_store && (args.mode != MODE_MASKED || slab0 + 32 <= m_valid) && slab0 < m_valid;
+                // One output box: this lane's 32 bytes of a 32-row x 32-byte box, staged in one of
+                // the warp's two buffers and written by a TMA bulk store.
+                auto put_box = [&](int col, uint4 w0, uint4 w1) {
+                    const uint32_t buf = stage_out + (nbox & 1u) * 1024u;
+                    if (nbox >= 2) {
+                        // the store that last read this buffer must be done reading it
+                        if (lane == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+                    }
+                    st_shared_v4(buf + lane * 32u, w0);
+                    st_shared_v4(buf + lane * 32u + 16u, w1);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tm_d, buf, col, slab0, t.g);
+                        bulk_commit_group();
+                    }
+                    ++nbox;
+                };
+                if (!args.out_f32) {
+                    // BF16 out: the whole row segment goes from TMEM to registers (packed) first,
+                    // so the accumulator is released before any store is issued and the stores
+                    // overlap the next tile's main loop.
+                    constexpr int CH = C::BN / 32 / C::EPI_COLS;
+                    static_assert(C::BN % (32 * C::EPI_COLS) == 0, "whole 32-column chunks per epilogue warp");
+                    uint32_t pk[CH * 16];
+#pragma unroll
+                    for (int i = 0; i < 2 * CH; ++i) {       // 16 columns at a time: fewer live registers
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x16(t_row + 16u * static_cast<uint32_t>(2 * ch_lo + i), r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) pk[8 * i + j] = zero_row ? 0u : pack_bf16x2(r[2 * j], r[2 * j + 1]);
+                    }
+                    tc_fence_before_sync();
+                    mbar_arrive(tempty_bar(acc));
+                    if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
+                    uint16_t* drow = static_cast<uint16_t*>(args.d) + row_off;
+#pragma unroll
+                    for (int i = 0; i < CH; ++i) {
+                        const int col0 = n0 + 32 * (ch_lo + i);
+                        const uint32_t* p = pk + 16 * i;
+                        if (slab_tma) {
+                            put_box(col0, make_uint4(p[0], p[1], p[2], p[3]), make_uint4(p[4], p[5], p[6], p[7]));
+                            put_box(col0 + 16, make_uint4(p[8], p[9], p[10], p[11]),
+                                    make_uint4(p[12], p[13], p[14], p[15]));
+                        } else if (write) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                if (col0 + 8 * j < N)
+                                    st_global_v4(drow + col0 + 8 * j,
+                                                 make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
+                        }
+                    }
+                    continue;   // the accumulator was released above
+                }
 #pragma unroll 1
                 for (int c = ch_lo; c < ch_hi; ++c) {
                     uint32_t r[32];
@@ -969,23 +1025,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                     // One box = 32 rows x 32 bytes: 16 BF16 or 8 FP32 columns (fully unrolled so
                     // that r and cv stay in registers).
-                    auto put_box = [&](int col, uint4 w0, uint4 w1) {
-                        const uint32_t buf = stage_out + (nbox & 1u) * 1024u;
-                        if (nbox >= 2) {
-                            // the store that last read this buffer must be done reading it
-                            if (lane == 0) bulk_wait_group_read<1>();
-                            __syncwarp();
-                        }
-                        st_shared_v4(buf + lane * 32u, w0);
-                        st_shared_v4(buf + lane * 32u + 16u, w1);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_3d(&tm_d, buf, col, slab0, t.g);
-                            bulk_commit_group();
-                        }
-                        ++nbox;
-                    };
                     const int col0 = n0 + 32 * c;
                     if (args.out_f32) {
 #pragma unroll
