@@ -552,36 +552,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0;   // stages issued in total (for the abort drain)
-            int sf_slot = 0;
-            uint32_t sf_phbits = 0;          // bit j: parity of scale slot j's empty barrier
-            int sf_last = -1;                // last scale slot loaded (for the abort drain)
-            uint32_t sf_last_par = 0;
             bool ok = true;
             for (int u = u_first; ok && u < total_units; u += u_step) {
                 const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
                 if (t.zero) continue;
                 const int ga = args.mode == MODE_MASKED ? t.g : 0;
                 for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
-                    if ((kb & 3) == 0) {
-                        // A new group of four K blocks: its packed scale words go to the next slot
-                        // of the scale ring once the MMAs of the slot's previous group are done.
-                        const uint32_t par = ((sf_phbits >> sf_slot) & 1u) ^ 1u;
-                        if (!wait_or_abort(sfempty_bar(sf_slot), par, misc + 1, args.err, args.timeout_ns,
-                                           SITE_SF_EMPTY)) {
-                            ok = false;
-                            break;
-                        }
-                        sf_phbits ^= 1u << sf_slot;
-                        const uint32_t sb = sffull_bar(sf_slot);
-                        mbar_arrive_expect_tx(sb, C::TX_SF);
-                        const int kp = t.kpoff + (kb >> 2);
-                        tma_load_3d(base + C::OFF_SFA + sf_slot * C::SFA_BYTES, &tm_sfa, sb, t.mb * C::TM, kp, ga);
-                        tma_load_3d(base + C::OFF_SFB + sf_slot * C::SFB_BYTES, &tm_sfb, sb, t.nb * C::BN, kp,
-                                    args.mode == MODE_K_GROUPED ? 0 : t.gb);
-                        sf_last = sf_slot;
-                        sf_last_par = par ^ 1u;
-                        if (++sf_slot == C::SF_SLOTS) sf_slot = 0;
-                    }
                     if (!wait_or_abort(empty_bar(s), ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_EMPTY)) {
                         ok = false;
                         break;
@@ -644,10 +620,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     --s;
                     const uint64_t t0 = global_timer_ns();
                     while (!mbar_try_wait(full_bar(s), ph) && global_timer_ns() - t0 < 100000000ull) {}
-                }
-                if (sf_last >= 0) {
-                    const uint64_t t0 = global_timer_ns();
-                    while (!mbar_try_wait(sffull_bar(sf_last), sf_last_par) && global_timer_ns() - t0 < 100000000ull) {}
                 }
             }
         }
@@ -755,13 +727,38 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // ring slot, re-lay them for tcgen05.cp, publish them to the async proxy and signal the
         // MMA issuers.  Every party uses each slot's barriers once per group, in group order, so
         // no wait is ever more than one phase from its barrier.
+        // Lane 0 also issues each group's scale loads, as soon as the group's ring slot is free
+        // (the MMAs of the group SF_SLOTS earlier are done): a whole group ahead of the A/B
+        // stages of the group, which is what hides the load latency and the re-layout.
         int sf_slot = 0;
         uint32_t sff_phbits = 0;
+        uint32_t sfe_phbits = 0;          // bit j: parity of scale slot j's empty barrier
+        int sf_last = -1;                 // last scale slot loaded (for the abort drain)
+        uint32_t sf_last_par = 0;
         bool ok = true;
         for (int u = u_first; ok && u < total_units; u += u_step) {
             const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
             if (t.zero) continue;
+            const int ga = args.mode == MODE_MASKED ? t.g : 0;
             for (int kb = t.kb_begin; kb < t.kb_end; kb += 4) {
+                if (lane == 0) {
+                    const uint32_t par = ((sfe_phbits >> sf_slot) & 1u) ^ 1u;
+                    if (wait_or_abort(sfempty_bar(sf_slot), par, misc + 1, args.err, args.timeout_ns, SITE_SF_EMPTY)) {
+                        const uint32_t sb = sffull_bar(sf_slot);
+                        mbar_arrive_expect_tx(sb, C::TX_SF);
+                        const int kp = t.kpoff + (kb >> 2);
+                        tma_load_3d(base + C::OFF_SFA + sf_slot * C::SFA_BYTES, &tm_sfa, sb, t.mb * C::TM, kp, ga);
+                        tma_load_3d(base + C::OFF_SFB + sf_slot * C::SFB_BYTES, &tm_sfb, sb, t.nb * C::BN, kp,
+                                    args.mode == MODE_K_GROUPED ? 0 : t.gb);
+                        sf_last = sf_slot;
+                        sf_last_par = (sff_phbits >> sf_slot) & 1u;
+                    }
+                }
+                sfe_phbits ^= 1u << sf_slot;
+                if (__shfl_sync(0xffffffffu, misc[1], 0)) {   // aborted (lane 0's wait gave up)
+                    ok = false;
+                    break;
+                }
                 if (!wait_fast(sffull_bar(sf_slot), (sff_phbits >> sf_slot) & 1u, misc + 1, args.err,
                                args.timeout_ns, SITE_SF_FULL)) {
                     ok = false;
@@ -779,6 +776,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (lane == 0) mbar_arrive(sfready_bar(sf_slot));
                 if (++sf_slot == C::SF_SLOTS) sf_slot = 0;
             }
+        }
+        if (lane == 0 && misc[1] && sf_last >= 0) {
+            // Abort: wait (bounded, short) until the last scale load issued has landed.
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(sffull_bar(sf_last), sf_last_par) && global_timer_ns() - t0 < 100000000ull) {}
         }
     } else if ((warp >= 2 && warp <= 5) || ((MH == 2 || C::EPI_COLS == 2) && warp >= 8)) {
         // ------------------------------------------------------------------ epilogue
