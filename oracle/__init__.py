@@ -44,12 +44,12 @@ Readings where the pages are silent (each listed in the design notes):
   P7  the exact sum is rounded once to BF16, round-to-nearest-even.
   P8  contiguous-layout padding rows (m_indices == -1) come out as +0.0.
   P9  masked-layout rows at or past masked_m[g] keep whatever D held before.
-  P13 C is added to the exact product sum and the result rounded once (to FP32
+  P18 C is added to the exact product sum and the result rounded once (to FP32
       or BF16); the GPU adds C to its FP32 accumulator, one more rounding.
-  P14 K-grouped scales: one FP32 scale per 128-row K block and per column of the
+  P19 K-grouped scales: one FP32 scale per 128-row K block and per column of the
       MN-major operand ([sum Kb][MN]), packed per group so that no packed word
       spans two groups; every ks[g] is a multiple of 128.
-  P15 FP4 weights: E2M1 codes packed two per byte, element 2i in the low nibble;
+  P20 FP4 weights: E2M1 codes packed two per byte, element 2i in the low nibble;
       their scales are the same packed UE8M0 1x128 words as FP8 B's (one per row
       and 128-wide K block) -- the pages fix neither the nibble order nor the
       FP4 scale granularity.
