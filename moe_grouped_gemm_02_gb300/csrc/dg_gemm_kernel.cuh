@@ -980,13 +980,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     constexpr int CH = C::BN / 32 / C::EPI_COLS;
                     static_assert(C::BN % (32 * C::EPI_COLS) == 0, "whole 32-column chunks per epilogue warp");
                     uint32_t pk[CH * 16];
+                    // 32 columns per TMEM load (half the round trips) where registers allow: with
+                    // 384 threads a thread has at most 168, so those kernels load 16 at a time.
+                    constexpr int LDC = C::THREADS <= 256 ? 32 : 16;
 #pragma unroll
-                    for (int i = 0; i < 2 * CH; ++i) {       // 16 columns at a time: fewer live registers
+                    for (int i = 0; i < 32 / LDC * CH; ++i) {
                         uint32_t r[32];
-                        tmem_ld_32x32b_x16(t_row + 16u * static_cast<uint32_t>(2 * ch_lo + i), r);
+                        if (LDC == 32) tmem_ld_32x32b_x32(t_row + 32u * static_cast<uint32_t>(ch_lo + i), r);
+                        else tmem_ld_32x32b_x16(t_row + 16u * static_cast<uint32_t>(2 * ch_lo + i), r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) pk[8 * i + j] = zero_row ? 0u : pack_bf16x2(r[2 * j], r[2 * j + 1]);
+                        for (int j = 0; j < LDC / 2; ++j)
+                            pk[LDC / 2 * i + j] = zero_row ? 0u : pack_bf16x2(r[2 * j], r[2 * j + 1]);
                     }
                     tc_fence_before_sync();
                     mbar_arrive(tempty_bar(acc));
