@@ -135,26 +135,37 @@ class DeviceWorkload:
             self.idx = t(w["masked_m"])
         self.N = N
 
-    def pack(self):
-        self.dg.dg_pack_sf_ue8m0(self.sfa_f, self.sfa, self.rows_a, 1)
+    def pack(self, io=None):
+        sfa_f = self.sfa_f if io is None else io["sfa_f"]
+        self.dg.dg_pack_sf_ue8m0(sfa_f, self.sfa, self.rows_a, 1)
         self.dg.dg_pack_sf_ue8m0(self.sfb_f, self.sfb, self.N, 128)
 
-    def gemm(self):
+    def gemm(self, io=None):
         dg = self.dg
+        a, d, idx = (self.a, self.d, getattr(self, "idx", None)) if io is None else (io["a"], io["d"], io["idx"])
         if self.kind == "dense":
-            dg.dg_fp8_gemm_nt(self.a, self.sfa, self.b, self.sfb, self.d)
+            dg.dg_fp8_gemm_nt(a, self.sfa, self.b, self.sfb, d)
         elif self.kind == "contiguous":
-            dg.dg_m_grouped_fp8_gemm_nt_contiguous(self.a, self.sfa, self.b, self.sfb, self.d, self.idx)
+            dg.dg_m_grouped_fp8_gemm_nt_contiguous(a, self.sfa, self.b, self.sfb, d, idx)
         else:
-            dg.dg_m_grouped_fp8_gemm_nt_masked(self.a, self.sfa, self.b, self.sfb, self.d, self.idx)
+            dg.dg_m_grouped_fp8_gemm_nt_masked(a, self.sfa, self.b, self.sfb, d, idx)
 
     # end-to-end: the step's inputs (activations, their FP32 scales, routing) come from pinned
-    # host memory and D goes back to pinned host memory; weights stay resident.
-    def setup_e2e(self):
+    # host memory and D goes back to pinned host memory; weights stay resident.  Two device
+    # sets of the per-step inputs and of D alternate between steps, so that one step's copies
+    # run while the previous step's GEMMs still use the other set.
+    def setup_e2e(self, dev):
         self.h_a = self.a.cpu().pin_memory()
         self.h_sfa = self.sfa_f.cpu().pin_memory()
         self.h_idx = self.idx.cpu().pin_memory() if self.kind != "dense" else None
         self.h_d = torch.empty(self.d.shape, dtype=self.d.dtype).pin_memory()
+        self.io = []
+        for j in range(2):
+            self.io.append({"a": torch.empty_like(self.a), "sfa_f": torch.empty_like(self.sfa_f),
+                            "idx": torch.empty_like(self.idx) if self.h_idx is not None else None,
+                            "d": torch.empty_like(self.d),
+                            "ev_h2d": torch.cuda.Event(), "ev_gemm": torch.cuda.Event(), "ev_d2h": torch.cuda.Event()})
+        self.e2e_n = 0
         h2d = self.h_a.numel() + self.h_sfa.numel() * 4 + (self.h_idx.numel() * 4 if self.h_idx is not None else 0)
         d2h = self.h_d.numel() * 2
         return h2d, d2h
@@ -162,30 +173,30 @@ class DeviceWorkload:
     def e2e_step(self, h2d_stream, compute_stream, d2h_stream):
         """One end-to-end pass: inputs from pinned host memory (h2d_stream), scale pack and
         GEMM (compute_stream), D back to pinned host memory (d2h_stream).  Events keep each
-        buffer from being overwritten while an earlier step still uses it."""
-        if not hasattr(self, "ev_h2d"):
-            self.ev_h2d = torch.cuda.Event()
-            self.ev_gemm = torch.cuda.Event()
-            self.ev_d2h = torch.cuda.Event()
-            self.ev_gemm.record(compute_stream)
-            self.ev_d2h.record(d2h_stream)
-        h2d_stream.wait_event(self.ev_gemm)              # the last GEMM is done reading the inputs
+        device set from being overwritten while an earlier step still uses it."""
+        io = self.io[self.e2e_n % 2]
+        if self.e2e_n < 2:
+            io["ev_gemm"].record(compute_stream)
+            io["ev_d2h"].record(d2h_stream)
+        self.e2e_n += 1
+        h2d_stream.wait_event(io["ev_gemm"])             # the GEMM two steps back is done with the set
         with torch.cuda.stream(h2d_stream):
-            self.a.copy_(self.h_a, non_blocking=True)
-            self.sfa_f.copy_(self.h_sfa, non_blocking=True)
+            io["a"].copy_(self.h_a, non_blocking=True)
+            io["sfa_f"].copy_(self.h_sfa, non_blocking=True)
             if self.h_idx is not None:
-                self.idx.copy_(self.h_idx, non_blocking=True)
-        self.ev_h2d.record(h2d_stream)
-        compute_stream.wait_event(self.ev_h2d)
-        compute_stream.wait_event(self.ev_d2h)           # D of the last step has been read back
+                io["idx"].copy_(self.h_idx, non_blocking=True)
+        io["ev_h2d"].record(h2d_stream)
+        compute_stream.wait_event(io["ev_h2d"])
+        compute_stream.wait_event(io["ev_d2h"])          # D of two steps back has been read back
         with torch.cuda.stream(compute_stream):
-            self.pack()
-            self.gemm()
-        self.ev_gemm.record(compute_stream)
-        d2h_stream.wait_event(self.ev_gemm)
+            self.pack(io)
+            self.gemm(io)
+        io["ev_gemm"].record(compute_stream)
+        d2h_stream.wait_event(io["ev_gemm"])
         with torch.cuda.stream(d2h_stream):
-            self.h_d.copy_(self.d, non_blocking=True)
-        self.ev_d2h.record(d2h_stream)
+            self.h_d.copy_(io["d"], non_blocking=True)
+        self.ev_d2h = io["ev_d2h"]
+        io["ev_d2h"].record(d2h_stream)
 
 
 # ---------------------------------------------------------------------------
@@ -375,7 +386,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     if not args.no_e2e:
         h2d = d2h = 0
         for dw in dws:
-            hb, db = dw.setup_e2e()
+            hb, db = dw.setup_e2e(dev)
             h2d += hb
             d2h += db
         h2d_stream, d2h_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
@@ -407,8 +418,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e_steps,
                "ms_per_step": round(e_ms / e_steps, 4),
                "how": "activations, their FP32 scales and routing copied from pinned host memory on one "
-                      "stream, scale pack + GEMM on the compute stream, D copied back on a third stream, "
-                      "overlapped across workloads; weights resident"}
+                      "stream, scale pack + GEMM on the compute stream, D copied back on a third stream; two "
+                      "device sets of inputs and D alternate between steps so copies overlap the previous "
+                      "step's GEMMs; weights resident"}
 
     next_rows = None if args.no_next else time_next_rows(dev, peaks)
 
