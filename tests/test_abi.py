@@ -100,3 +100,31 @@ def test_fp4_validation(lib):
     assert c(GOOD, GOOD, ODD16, GOOD, GOOD, GOOD, 256, 512, 1024, 4, None) == 3
     m = lib.dg_m_grouped_fp8_fp4_gemm_nt_masked
     assert m(GOOD, GOOD, GOOD, GOOD, GOOD, None, 4, 256, 512, 1024, None) == 1
+
+
+def test_layout_gemm_validation(lib):
+    f = lib.dg_fp8_gemm
+    F32, BF16 = 1, 0
+    assert f(GOOD, GOOD, GOOD, GOOD, None, GOOD, 128, 512, 1024, 4, BF16, None) == 1     # no such layout
+    assert f(GOOD, GOOD, GOOD, GOOD, GOOD, GOOD, 128, 512, 1024, 0, BF16, None) == 1     # C needs FP32 D
+    assert f(GOOD, GOOD, GOOD, GOOD, None, GOOD, 128, 512, 1024, 0, 2, None) == 1        # out flag 0/1
+    assert f(GOOD, GOOD, GOOD, GOOD, None, GOOD, 120, 512, 1024, 2, F32, None) == 2     # TN: M % 16
+    assert f(GOOD, GOOD, GOOD, GOOD, None, GOOD, 128, 520, 1024, 1, F32, None) == 2     # NN: N % 16
+    assert f(GOOD, GOOD, GOOD, GOOD, ODD, GOOD, 128, 512, 1024, 0, F32, None) == 3      # misaligned C
+    assert f(GOOD, GOOD, GOOD, GOOD, None, GOOD, 0, 512, 1024, 3, F32, None) == 0       # empty
+
+
+def test_k_grouped_validation(lib):
+    f = lib.dg_k_grouped_fp8_gemm_tn_contiguous
+    assert f(GOOD, GOOD, GOOD, GOOD, None, GOOD, None, 4, 256, 512, 1024, None) == 1   # no ks
+    assert f(GOOD, GOOD, GOOD, GOOD, None, GOOD, GOOD, 0, 256, 512, 1024, None) == 1   # G == 0
+    assert f(GOOD, GOOD, GOOD, GOOD, None, GOOD, GOOD, 4, 250, 512, 1024, None) == 2   # M % 16
+    assert f(GOOD, GOOD, GOOD, GOOD, None, GOOD, GOOD, 4, 256, 512, 1000, None) == 2   # sum_K % 128
+    assert f(GOOD, GOOD, GOOD, GOOD, None, GOOD, GOOD, 5000, 256, 512, 1024, None) == 2  # too many groups
+    assert f(GOOD, GOOD, GOOD, GOOD, ODD, GOOD, GOOD, 4, 256, 512, 1024, None) == 3    # misaligned C
+    assert f(GOOD, GOOD, GOOD, GOOD, None, GOOD, GOOD, 4, 0, 512, 1024, None) == 0     # empty
+    p = lib.dg_pack_sf_ue8m0_k_grouped
+    assert p(GOOD, GOOD, None, 4, 256, 1024, None) == 1                                 # no ks
+    assert p(GOOD, GOOD, GOOD, 4, 256, 1000, None) == 2                                 # sum_K % 128
+    assert p(GOOD, ODD, GOOD, 4, 256, 1024, None) == 3                                  # misaligned out
+    assert p(GOOD, GOOD, GOOD, 4, 0, 1024, None) == 0                                   # empty
