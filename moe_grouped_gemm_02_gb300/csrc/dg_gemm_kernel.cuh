@@ -1001,7 +1001,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     for (int i = 0; i < CH; ++i) {
                         const int col0 = n0 + 32 * (ch_lo + i);
                         const uint32_t* p = pk + 16 * i;
-                        if (slab_tma) {
+                        // With two accumulators the stores never hold up the next tile's MMAs; they
+                        // only end the CTA's last tile, where plain stores finish sooner than the
+                        // chain of staged boxes.
+                        if (slab_tma && C::ACC == 1) {
                             put_box(col0, make_uint4(p[0], p[1], p[2], p[3]), make_uint4(p[4], p[5], p[6], p[7]));
                             put_box(col0 + 16, make_uint4(p[8], p[9], p[10], p[11]),
                                     make_uint4(p[12], p[13], p[14], p[15]));
