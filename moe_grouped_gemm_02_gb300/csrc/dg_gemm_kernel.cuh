@@ -931,12 +931,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 continue;
             }
+            float4 cv_next[8];    // FP32 with C: the next chunk's C values
             if (use_c && ((t.hmask >> my_half) & 1u)) {
-                // Ask L2 for this thread's C segment while the tile's main loop still runs.
+                // Ask L2 for this thread's C segment, and load its first chunk, while the tile's
+                // main loop still runs.
                 const int row = row_of(my_half);
                 const int c0 = n0 + 32 * ch_lo, c1 = min(N, n0 + 32 * ch_hi);
-                if (row < m_valid && c1 > c0)
+                if (row < m_valid && c1 > c0) {
                     prefetch_l2(args.c + roff_of(row) + c0, static_cast<uint32_t>(c1 - c0) * 4u);
+                    load_c_chunk(args, roff_of(row), c0, N, 32, cv_next);
+                }
             }
             if (!wait_or_abort(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
             tc_fence_after_sync();
@@ -1018,6 +1022,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                     continue;   // the accumulator was released above
                 }
+                // FP32: C runs one chunk ahead in registers (the first chunk's C was loaded
+                // before the wait for the accumulator), so its latency overlaps the TMEM loads
+                // and the stores of the chunk before.
 #pragma unroll 1
                 for (int c = ch_lo; c < ch_hi; ++c) {
                     uint32_t r[32];
@@ -1026,8 +1033,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     if (half_chunk) tmem_ld_32x32b_x16(t_row + 32u * c, r);
                     else tmem_ld_32x32b_x32(t_row + 32u * c, r);
                     float4 cv[8];
-                    // C's loads go out before the wait for the TMEM load, so the two overlap
-                    if (use_c && write) load_c_chunk(args, row_off, n0 + 32 * c, N, ncols, cv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) cv[j] = cv_next[j];
+                    if (use_c && write && c + 1 < ch_hi) load_c_chunk(args, row_off, n0 + 32 * (c + 1), N, 32, cv_next);
                     tmem_wait_ld();
                     if (!slab_tma) {
                         if (write) store_row_chunk(args, row_off, n0 + 32 * c, N, r, ncols, zero_row, use_c ? cv : nullptr);
