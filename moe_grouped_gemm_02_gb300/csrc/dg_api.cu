@@ -50,7 +50,8 @@ int pdl_enabled() {
 const KernelConfig* const* all_configs(int* n) {
     static const KernelConfig* cfgs[] = {&config_bn256_s4_a1(), &config_bn224_s4_a2(),
                                          &config_bn192_s5_a2(), &config_bn128_s6_a2(), &config_bn128_s4_a2(), &config_bn64_s8_a2(),
-                                         &config_bn32_s8_a2(), &config_bn224_s3_m2(), &config_bn192_s3_m2()};
+                                         &config_bn32_s8_a2(), &config_bn224_s3_m2(), &config_bn192_s3_m2(),
+                                         &config_bn208_s3_m2()};
     *n = static_cast<int>(sizeof(cfgs) / sizeof(cfgs[0]));
     return cfgs;
 }

@@ -33,6 +33,8 @@
 // loop, waits (bounded) for copies it still has in flight, frees its TMEM and returns.
 #pragma once
 
+#include <type_traits>
+
 #include "dg_internal.h"
 #include "dg_ptx.cuh"
 
@@ -61,7 +63,8 @@ struct GemmCfg {
     static constexpr int EPI_THREADS = 128 * MH * EPI_COLS;
     static_assert(MH == 1 || MH == 2, "a tile has one or two 128-row halves");
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 16 in [32, 256]");
-    static_assert(BN % 32 == 0 || (ACC == 1 && MH == 1), "accumulators must start on 32-column boundaries");
+    // Accumulators start on 32-column boundaries: BN columns each, ACC_STRIDE apart.
+    static constexpr int ACC_STRIDE = (BN + 31) / 32 * 32;
     static constexpr int SFB_CHUNKS = (BN + 127) / 128;   // 128-row scale chunks of a B tile
     static constexpr int A_BYTES = TM * BK;
     static constexpr int B_BYTES = BN * BK;
@@ -80,7 +83,7 @@ struct GemmCfg {
     // then per slot and per issuer 4 columns of A scales and 4 per 128-row chunk of B scales.
     static constexpr int SF_COLS = 4 + 4 * SFB_CHUNKS;
     static constexpr int SF_SLOTS = MH == 2 ? 2 : 3;
-    static constexpr int TMEM_USED = ACC * MH * BN + SF_SLOTS * MH * SF_COLS;
+    static constexpr int TMEM_USED = ACC * MH * ACC_STRIDE + SF_SLOTS * MH * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64
                                    : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
@@ -660,7 +663,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((acc * MH + h) * C::BN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((acc * MH + h) * C::ACC_STRIDE);
                 for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
                     if ((kb & 3) == 0) {
                         // First K block of a group: copy the group's re-laid scale words from its
@@ -674,7 +677,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         sfr_phbits ^= 1u << sf_slot;
                         tc_fence_after_sync();
                         sfa_t = tmem_base +
-                                static_cast<uint32_t>(C::ACC * MH * C::BN + (sf_slot * MH + h) * C::SF_COLS);
+                                static_cast<uint32_t>(C::ACC * MH * C::ACC_STRIDE + (sf_slot * MH + h) * C::SF_COLS);
                         sfb_t = sfa_t + 4u;
                         if (active) {
                             tc_cp_32x128b_warpx4(sfa_t, smem_desc_sf_chunk(base + C::OFF_SFA + sf_slot * C::SFA_BYTES +
@@ -846,7 +849,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 if (!wait_or_abort(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
                 tc_fence_after_sync();
-                const uint32_t t_row = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * C::BN);
+                const uint32_t t_row = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * C::ACC_STRIDE);
                 if (warp_send) {
                     if (!wait_cluster_or_abort(redempty_bar, red_eph ^ 1u, misc + 1, args.err, args.timeout_ns,
                                                SITE_RED_EMPTY))
@@ -952,7 +955,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 row_state(row, write, zero_row);
                 const size_t row_off = roff_of(row);
                 const uint32_t t_row =
-                    tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>((acc * MH + h) * C::BN);
+                    tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>((acc * MH + h) * C::ACC_STRIDE);
                 // The warp's 32 rows go out as TMA boxes unless some of them must stay untouched
                 // (masked mode past masked_m[g]); rows past D's extent are clipped by the map.
                 const int slab0 = row - static_cast<int>(lane);
@@ -981,40 +984,49 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     // BF16 out: the whole row segment goes from TMEM to registers (packed) first,
                     // so the accumulator is released before any store is issued and the stores
                     // overlap the next tile's main loop.
-                    constexpr int CH = C::BN / 32 / C::EPI_COLS;
-                    static_assert(C::BN % (32 * C::EPI_COLS) == 0, "whole 32-column chunks per epilogue warp");
-                    uint32_t pk[CH * 16];
+                    // The segment is handled in 16-column pieces (a BN that is not a multiple of 32
+                    // ends in a single one).
+                    constexpr int NP = C::BN / 16 / C::EPI_COLS;
+                    static_assert(C::BN % (16 * C::EPI_COLS) == 0, "whole 16-column pieces per epilogue warp");
+                    const int pc0 = 2 * ch_lo;                   // first piece of this thread's segment
+                    uint32_t pk[NP * 8];
                     // 32 columns per TMEM load (half the round trips) where registers allow: with
                     // 384 threads a thread has at most 168, so those kernels load 16 at a time.
                     constexpr int LDC = C::THREADS <= 256 ? 32 : 16;
-#pragma unroll
-                    for (int i = 0; i < 32 / LDC * CH; ++i) {
+                    auto load_pieces = [&](int i, auto width) {   // pieces i (and i + 1 when 32 wide)
                         uint32_t r[32];
-                        if (LDC == 32) tmem_ld_32x32b_x32(t_row + 32u * static_cast<uint32_t>(ch_lo + i), r);
-                        else tmem_ld_32x32b_x16(t_row + 16u * static_cast<uint32_t>(2 * ch_lo + i), r);
+                        const uint32_t col = t_row + 16u * static_cast<uint32_t>(pc0 + i);
+                        if (decltype(width)::value == 32) tmem_ld_32x32b_x32(col, r);
+                        else tmem_ld_32x32b_x16(col, r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < LDC / 2; ++j)
-                            pk[LDC / 2 * i + j] = zero_row ? 0u : pack_bf16x2(r[2 * j], r[2 * j + 1]);
+                        for (int j = 0; j < decltype(width)::value / 2; ++j)
+                            pk[8 * i + j] = zero_row ? 0u : pack_bf16x2(r[2 * j], r[2 * j + 1]);
+                    };
+                    if (LDC == 32) {
+#pragma unroll
+                        for (int i = 0; i < NP / 2; ++i) load_pieces(2 * i, std::integral_constant<int, 32>());
+                        if (NP % 2) load_pieces(NP - 1, std::integral_constant<int, 16>());
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < NP; ++i) load_pieces(i, std::integral_constant<int, 16>());
                     }
                     tc_fence_before_sync();
                     mbar_arrive(tempty_bar(acc));
                     if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
                     uint16_t* drow = static_cast<uint16_t*>(args.d) + row_off;
 #pragma unroll
-                    for (int i = 0; i < CH; ++i) {
-                        const int col0 = n0 + 32 * (ch_lo + i);
-                        const uint32_t* p = pk + 16 * i;
+                    for (int i = 0; i < NP; ++i) {
+                        const int col0 = n0 + 16 * (pc0 + i);
+                        const uint32_t* p = pk + 8 * i;
                         // With two accumulators the stores never hold up the next tile's MMAs; they
                         // only end the CTA's last tile, where plain stores finish sooner than the
                         // chain of staged boxes.
                         if (slab_tma && C::ACC == 1) {
                             put_box(col0, make_uint4(p[0], p[1], p[2], p[3]), make_uint4(p[4], p[5], p[6], p[7]));
-                            put_box(col0 + 16, make_uint4(p[8], p[9], p[10], p[11]),
-                                    make_uint4(p[12], p[13], p[14], p[15]));
                         } else if (write) {
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
+                            for (int j = 0; j < 2; ++j)
                                 if (col0 + 8 * j < N)
                                     st_global_v4(drow + col0 + 8 * j,
                                                  make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));

@@ -77,6 +77,7 @@ const KernelConfig& config_bn64_s8_a2();
 const KernelConfig& config_bn32_s8_a2();
 const KernelConfig& config_bn224_s3_m2();
 const KernelConfig& config_bn192_s3_m2();
+const KernelConfig& config_bn208_s3_m2();
 
 cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb, int Kb, int Kp,
                            int mn_al, int gran_mn, int pdl, cudaStream_t stream);

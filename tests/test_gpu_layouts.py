@@ -125,6 +125,7 @@ def forced(monkeypatch):
     ("config_bn224_s3_m2", None, "tt"),     # 256-row tiles with an MN-major A
     ("config_bn192_s3_m2", None, "tt"),
     ("config_bn64_s8_a2", 8, "tt"),
+    ("config_bn208_s3_m2", None, "tn"),     # 208 columns: a 16-column epilogue tail, 224-column accumulator stride
 ])
 def test_forced_plans_with_layouts(forced, cfg, split, layout):
     forced(cfg, split)

@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 CONFIGS = ["config_bn256_s4_a1", "config_bn224_s4_a2", "config_bn192_s5_a2", "config_bn128_s6_a2",
            "config_bn128_s4_a2", "config_bn64_s8_a2", "config_bn32_s8_a2", "config_bn224_s3_m2",
-           "config_bn192_s3_m2"]
+           "config_bn192_s3_m2", "config_bn208_s3_m2"]
 
 
 def _call_or_skip(fn, *args):
@@ -161,7 +161,7 @@ def test_grouped_pair_multicast(cfg, few_sms, monkeypatch):
     assert_within_tolerance(got[rows], want[rows], f"masked pair {cfg}")
 
 
-@pytest.mark.parametrize("cfg", ["config_bn224_s3_m2", "config_bn192_s3_m2"])
+@pytest.mark.parametrize("cfg", ["config_bn224_s3_m2", "config_bn192_s3_m2", "config_bn208_s3_m2"])
 def test_contiguous_256_row_tiles_straddling_experts(cfg, few_sms, monkeypatch):
     # 256-row tiles (two 128-row halves): expert 0 has one block and expert 1 two, so the first
     # tile holds two experts and runs as two passes; then a trailing all-padding tile.
