@@ -103,3 +103,58 @@ def test_masked_moe_full():
     rows = np.arange(max_m)[None, :] < w["masked_m"][:, None]
     assert np.array_equal(got[~rows], want[~rows])
     assert_within_tolerance(got[rows], want[rows], "masked full")
+
+
+# ---------------------------------------------------------------------------
+# The shapes the benchmark times beside the step, at full size
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("shape_idx", range(len(synth.DECODE_SHAPES)))
+def test_fp8_fp4_decode_shapes_full(shape_idx):
+    M, N, K = synth.DECODE_SHAPES[shape_idx]
+    w = synth.with_fp4_b(synth.make_dense(M, N, K, seed=20 + shape_idx, a_outliers=True), seed=20 + shape_idx)
+    sfa = oracle.pack_sf_ue8m0(w["sfa"], M, 1)[0]
+    sfb = oracle.pack_sf_ue8m0(w["sfb_fp4"], N, 1)[0]
+    d = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    dg.dg_fp8_fp4_gemm_nt(to_dev(w["a"]), to_dev(sfa), to_dev(w["b_fp4"]), to_dev(sfb), d)
+    dg.dg_check_device_error()
+    assert_within_tolerance(bits(d), oracle.fp8_fp4_gemm_nt(w["a"], sfa, w["b_fp4"], sfb), f"fp8xfp4 {M}x{N}x{K}")
+
+
+def test_fp8_fp4_masked_full():
+    m = synth.MASKED
+    w = synth.with_fp4_b(synth.make_masked(m["G"], m["max_m"], m["N"], m["K"], seed=0), seed=0)
+    G, max_m, N = m["G"], m["max_m"], m["N"]
+    sfa = oracle.pack_sf_ue8m0(w["sfa"], max_m, 1)
+    sfb = oracle.pack_sf_ue8m0(w["sfb_fp4"], N, 1)
+    d = torch.full((G, max_m, N), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
+    dg.dg_m_grouped_fp8_fp4_gemm_nt_masked(to_dev(w["a"]), to_dev(sfa), to_dev(w["b_fp4"]), to_dev(sfb), d,
+                                          to_dev(w["masked_m"]))
+    dg.dg_check_device_error()
+    prior = np.full((G, max_m, N), synth.SENTINEL_BF16, np.uint16)
+    want = oracle.m_grouped_fp8_fp4_gemm_nt_masked(w["a"], sfa, w["b_fp4"], sfb, w["masked_m"], prior)
+    got = bits(d)
+    rows = np.arange(max_m)[None, :] < w["masked_m"][:, None]
+    assert np.array_equal(got[~rows], want[~rows])
+    assert_within_tolerance(got[rows], want[rows], "fp8xfp4 masked full")
+
+
+def test_nn_layout_fp32_accumulate_prefill_sampled_rows():
+    # The prefill shape in the NN layout, D += A B^T in FP32 in place: sampled rows of every
+    # 128-row block against the oracle (which adds C exactly).
+    M, N, K = synth.PREFILL_SHAPE
+    w = synth.make_dense(M, N, K, seed=11, b_std=0.02)
+    sfa = oracle.pack_sf_ue8m0(w["sfa"], M, 1)[0]
+    sfb = oracle.pack_sf_ue8m0(w["sfb"], N, 128)[0]
+    b_nn = np.ascontiguousarray(w["b"].T)                          # [K, N]
+    c = synth.normal((M, N), 11, "d_fill", std=0.5)
+    d = to_dev(c)
+    dg.dg_fp8_gemm(to_dev(w["a"]), to_dev(sfa), to_dev(b_nn), to_dev(sfb), d, layout="nn", c=d)
+    dg.dg_check_device_error()
+    got = d.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    rows = _sample_rows(M, 2, seed=11)
+    want = oracle.fp8_gemm(w["a"][rows], oracle.pack_sf_ue8m0(w["sfa"][rows], len(rows), 1)[0], b_nn, sfb,
+                           layout="nn", c=c[rows], out="f32")
+    from tests._parity import assert_close_f32
+    assert_close_f32(got[rows], want, "nn f32 accumulate prefill")
