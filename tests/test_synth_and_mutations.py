@@ -173,3 +173,98 @@ def test_mutation_padding_not_zeroed(monkeypatch):
         return out
     monkeypatch.setattr(oracle, "m_grouped_fp8_gemm_nt_contiguous", leaky)
     _fails(pins.test_contiguous_equals_dense_per_expert)
+
+
+# ---------------------------------------------------------------------------
+# Planted mistakes in the layout, K-grouped, FP8 x FP4 and quantisation parts of the oracle
+# ---------------------------------------------------------------------------
+
+def _fails_any(fn, *args):
+    """A pin catches the mistake by failing an assertion or by refusing the data outright."""
+    with pytest.raises((AssertionError, ValueError, IndexError)):
+        fn(*args)
+
+
+def test_mutation_layout_transpose_dropped(monkeypatch):
+    monkeypatch.setattr(R, "_k_major", lambda codes, stored_mn_major: np.asarray(codes, dtype=np.uint8))
+    _fails_any(pins.test_fp8_gemm_layouts_and_accumulation_brute_force, "tn")
+    _fails_any(pins.test_fp8_gemm_layouts_and_accumulation_brute_force, "nn")
+
+
+def test_mutation_c_subtracted(monkeypatch):
+    orig = R.fp8_gemm
+
+    def minus_c(a, sfa, b, sfb, layout="nt", c=None, out="bf16"):
+        return orig(a, sfa, b, sfb, layout, None if c is None else -np.asarray(c), out)
+    monkeypatch.setattr(oracle, "fp8_gemm", minus_c)
+    _fails(pins.test_fp8_gemm_layouts_and_accumulation_brute_force, "nt")
+
+
+def test_mutation_f32_out_rounded_to_bf16(monkeypatch):
+    def via_bf16(x):
+        return R.bf16_bits_to_float(R.bf16_round_bits(x)).astype(np.float32)
+    monkeypatch.setattr(R, "f32_round", via_bf16)
+    _fails(pins.test_fp8_gemm_layouts_and_accumulation_brute_force, "nt")
+    _fails(pins.test_k_grouped_gemm_brute_force)
+
+
+def test_mutation_k_group_offsets_inclusive(monkeypatch):
+    orig = R.k_group_offsets
+
+    def inclusive(ks):
+        koff, kboff, kpoff = orig(ks)
+        ks = np.asarray(ks, dtype=np.int64)
+        return koff + ks, kboff, kpoff                     # groups start at their own end
+    monkeypatch.setattr(R, "k_group_offsets", inclusive)
+    _fails_any(pins.test_k_grouped_gemm_brute_force)
+
+
+def test_mutation_k_grouped_pack_spans_groups(monkeypatch):
+    def one_pack(sf, mn, ks):
+        # wrong reading: the groups' K blocks packed as one run, words spanning group boundaries
+        return R.pack_sf_ue8m0(np.asarray(sf, np.float32)[:, :mn].T[None], mn, 1)[0]
+    monkeypatch.setattr(oracle, "pack_sf_ue8m0_k_grouped", one_pack)
+    _fails_any(pins.test_k_grouped_pack_brute_force)
+
+
+def test_mutation_e2m1_bias(monkeypatch):
+    t = R._E2M1 * 2.0                                      # exponent bias 0 instead of 1
+    monkeypatch.setattr(R, "_E2M1", t)
+    monkeypatch.setattr(oracle, "e2m1_decode_table", lambda: t.copy())
+    _fails(pins.test_e2m1_table_is_the_format)
+    _fails(pins.test_fp8_fp4_gemm_brute_force)
+
+
+def test_mutation_fp4_nibble_order(monkeypatch):
+    def swapped(packed):
+        p = np.asarray(packed, dtype=np.uint8)
+        out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+        out[..., 0::2] = p >> 4
+        out[..., 1::2] = p & 0xF
+        return out
+    monkeypatch.setattr(R, "fp4_unpack", swapped)
+    monkeypatch.setattr(oracle, "fp4_unpack", swapped)
+    _fails(pins.test_fp4_unpack_nibble_order)
+    _fails(pins.test_fp8_fp4_gemm_brute_force)
+
+
+def test_mutation_quantiser_ties_away(monkeypatch):
+    orig = R.e4m3_encode_rne
+
+    def ties_away(v):
+        v = np.asarray(v, dtype=np.float64)
+        # nudge every value a hair away from zero, which turns ties into round-half-away
+        return orig(np.where(np.abs(v) < 448, v * (1 + 2.0 ** -40), v))
+    monkeypatch.setattr(oracle, "e4m3_encode_rne", ties_away)
+    _fails(pins.test_e4m3_encode_matches_torch_cast_on_float32)
+
+
+def test_mutation_quantiser_exponent_boundary(monkeypatch):
+    orig = R.block_scale_exponent
+
+    def strict(amax):
+        e = orig(amax)
+        a = np.asarray(amax, dtype=np.float64)
+        return np.where(np.ldexp(448.0, e) == a, e + 1, e)   # 448 * 2**e == amax wrongly bumped
+    monkeypatch.setattr(oracle, "block_scale_exponent", strict)
+    _fails(pins.test_block_scale_exponent_definition)
