@@ -556,6 +556,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t ph = 0;
             uint32_t issued = 0;   // stages issued in total (for the abort drain)
             bool ok = true;
+            const bool keep_b = args.mode == MODE_CONTIGUOUS || (args.mode == MODE_DENSE && args.num_m_blocks > 2);
+            const uint64_t b_policy = policy_evict_last();
             for (int u = u_first; ok && u < total_units; u += u_step) {
                 const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
                 if (t.zero) continue;
@@ -597,7 +599,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             tma_load_3d(base + C::OFF_B + s * C::B_STAGE + j * (128 * BK), &tm_b, fb,
                                         t.nb * C::BN + j * 128, kx, gbz);
                     } else if (!pair) {
-                        tma_load_3d(base + C::OFF_B + s * C::B_STAGE, &tm_b, fb, kx, t.nb * C::BN, gbz);
+                        // B tiles are re-read by every m-tile of their group: keep them in L2
+                        if (keep_b) tma_load_3d_hint(base + C::OFF_B + s * C::B_STAGE, &tm_b, fb, kx, t.nb * C::BN, gbz,
+                                                     b_policy);
+                        else tma_load_3d(base + C::OFF_B + s * C::B_STAGE, &tm_b, fb, kx, t.nb * C::BN, gbz);
                     } else {
                         // The B map's box is half a tile; with multicast each CTA of the pair loads
                         // one half into both CTAs, otherwise each loads both halves itself.
