@@ -1,23 +1,29 @@
-// The FP8 block-scaled GEMM kernel family for sm_103a: D = A @ B^T, E4M3 operands, UE8M0
-// scales (one per row per 128-wide K block), FP32 accumulation in tensor memory, BF16 out.
+// The FP8 block-scaled GEMM kernel family for sm_103a: D = C + A @ B^T, E4M3 (or, for B,
+// E2M1) operands, UE8M0 scales (one per row per 128-wide K block), FP32 accumulation in
+// tensor memory, BF16 or FP32 out.
 //
 // The method is the one the DeepGEMM pages describe (README "Interface / Notes": fine-grained
-// scaled FP8 GEMM with packed UE8M0 scale factors on SM100; article sections 4.1 and 5.2:
-// TMA loads of both operands, warp specialization into loader / tensor-core / store roles,
-// section 7: a unified tile scheduler for L2 reuse).  The Hopper design on the pages promotes
-// partial sums to CUDA-core registers to apply the scales; here the tcgen05 block-scaled MMA
-// applies the UE8M0 scales in hardware and accumulates in TMEM, so there is no promotion.
+// scaled FP8 GEMM with packed UE8M0 scale factors on SM100, in the NT/TN/NN/TT layouts; article
+// sections 4.1 and 5.2: TMA loads of both operands, warp specialization into loader /
+// tensor-core / store roles, section 7: a unified tile scheduler for L2 reuse).  The Hopper
+// design on the pages promotes partial sums to CUDA-core registers to apply the scales; here
+// the tcgen05 block-scaled MMA applies the UE8M0 scales in hardware and accumulates in TMEM,
+// so there is no promotion.
 //
 // One CTA per SM, persistent over output tiles of (128 * MH) x BN, warp-specialised:
-//   warp 0        TMA producer: A tile [128*MH x 128], B tile [BN x 128] (128-byte swizzle)
-//                 into an S-stage ring; the packed scale words of every group of four K
-//                 blocks into a separate 3-slot scale ring.
+//   warp 0        TMA producer: A tile [128*MH x 128 K], B tile [BN x 128 K] (128-byte swizzle;
+//                 MN-major operands in boxes of 128 MN x 128 K; E2M1 B unpacked by the TMA)
+//                 into an S-stage ring.
 //   warp 1 (+7)   MMA issuers, one lane each: kind::mxf8f6f4 block-scaled MMAs (K = 32) into
 //                 TMEM; with MH = 2 each issuer owns one 128-row half of the tile, so two
 //                 instruction streams keep the tensor pipe fed.  Warp 1 also owns TMEM.
-//   warps 2-5     epilogue: TMEM -> registers -> BF16 -> global, one output row per thread
-//   (+8-11)       (with MH = 2 a second set of four writes the second 128-row half).
-//   warp 6        re-lays scale words for tcgen05.cp.
+//   warp 6        the scale warp: loads the packed scale words of every group of four K
+//                 blocks into a 2-3-slot ring as soon as a slot frees (a group ahead of the
+//                 operands) and re-lays them for tcgen05.cp.
+//   warps 2-5     epilogue, one output row per thread: TMEM -> registers (BF16 rows packed in
+//   (+8-11)       registers, then TMEM released) -> shared-memory boxes -> TMA bulk stores;
+//                 with MH = 2 the second set writes the second 128-row half, with MH = 1 and
+//                 one accumulator the two sets split the columns.
 // With MH = 1 the accumulator can be double-buffered in TMEM (ACC = 2) so that the epilogue
 // of one tile overlaps the main loop of the next.  MH = 2 halves the operand bytes each SM
 // ingests per multiply-add (one B tile serves 256 rows), the limit for large GEMMs.
@@ -25,7 +31,8 @@
 // Modes (runtime): dense; M-grouped contiguous (each 128-row block takes the expert of its
 // first row from m_indices, padding rows are written as +0.0); M-grouped masked (the
 // per-group valid-row counts are read on the device, only valid rows are computed and
-// written).  Options (runtime, MH = 1): split-K over a cluster of 2 or 4 CTAs reduced through
+// written); K-grouped (per-group K ranges read on the device, MN-major operands, FP32 out).
+// Options (runtime, MH = 1): split-K over a cluster of 2, 4 or 8 CTAs reduced through
 // distributed shared memory; CTA pairs sharing B tiles by TMA multicast.
 //
 // Every barrier wait is bounded (GemmArgs::timeout_ns).  On timeout the kernel records the
