@@ -282,6 +282,24 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# Ranks (one process per GPU under torchrun; independent replicas, weak scaling)
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's time: the whole job ends when its last replica does."""
+    if world <= 1:
+        return x
+    t = torch.tensor([float(x)], device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, ms: float) -> float:
+    """All ranks' work over the slowest rank's time: every replica runs the same suite."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
+# ---------------------------------------------------------------------------
 # Arms
 # ---------------------------------------------------------------------------
 
@@ -345,14 +363,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     clocks = sampler.stop()
     dg.dg_check_device_error()
     total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     dom_ms = statistics.mean(ev[k][dom][0].elapsed_time(ev[k][dom][1]) for k in range(args.steps))
 
     flops_step = sum(w["flops"] for w in ws)
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops_step, args.steps, world, total_ms)
     peaks = read_peaks()
     timed_s = total_ms * 1e-3
     bf16 = peaks["bf16_sustained"] if timed_s >= 1.0 else peaks["bf16"]
@@ -410,11 +425,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         a1.record(stream)
         torch.cuda.synchronize()
         e_ms = a0.elapsed_time(a1)
-        if world > 1:
-            tt = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(tt.item())
-        e2e = {"value": round(world * flops_step * e_steps / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+        e_ms = max_over_ranks(e_ms, world, dev)
+        e2e = {"value": round(whole_job_tflops(flops_step, e_steps, world, e_ms), 2), "unit": "TFLOPS",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e_steps,
                "ms_per_step": round(e_ms / e_steps, 4),
                "how": "activations, their FP32 scales and routing copied from pinned host memory on one "
