@@ -188,7 +188,6 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                  int extra_ints, int b_mn, int b_fp4) {
     int n = 0;
     const KernelConfig* const* cfgs = all_configs(&n);
-    const int ngroups = (kblocks + 3) / 4;
     // DG_FORCE_CONFIG=<name>, DG_FORCE_SPLIT=<1|2|4>, DG_FORCE_PAIR=<0|1> pin the plan (tuning).
     const char* force_cfg = std::getenv("DG_FORCE_CONFIG");
     const char* force_split = std::getenv("DG_FORCE_SPLIT");
@@ -218,7 +217,7 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                 // Masked groups are filled to an unknown, typically partial, depth: 256-row tiles
                 // would mostly compute padding unless the groups are deep.
                 if (c->mh > 1 && mode == MODE_MASKED && rows < 512 && !force_cfg) continue;
-                if (split > 1 && (ngroups < split || c->bn % 32 != 0)) continue;
+                if (split > 1 && (kblocks < split || c->bn % 32 != 0)) continue;
                 if (c->smem_bytes(extra_ints, split, 0) > static_cast<size_t>(st.max_smem)) continue;
                 const int tma_store = split == 1 && c->smem_bytes(extra_ints, 1, 1) <= static_cast<size_t>(st.max_smem);
                 int cap = sms;
@@ -232,7 +231,7 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                 const long long m_units = (pair || c->mh == 2) ? (m_blocks_total + 1) / 2 : m_blocks_total;
                 const long long tiles = m_units * ((N + c->bn - 1) / c->bn);
                 const long long waves = (tiles + cap - 1) / cap;
-                const double kb_per = 4.0 * ((ngroups + split - 1) / split);
+                const double kb_per = static_cast<double>((kblocks + split - 1) / split);
                 // an MN-major B arrives in whole 128-column boxes
                 const double b_rows = b_mn ? 128.0 * ((c->bn + 127) / 128) : (pair ? c->bn / 2 : c->bn);
                 const double tma = 2.2 * (128.0 * c->mh + b_rows);

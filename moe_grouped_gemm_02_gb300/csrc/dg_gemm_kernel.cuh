@@ -545,16 +545,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     tc_fence_after_sync();
 
     const uint32_t tmem_base = misc[0];
-    // Split-K: the CTAs of a cluster take the same tiles; CTA `crank` covers K-block groups
-    // [crank * ngroups / split, (crank + 1) * ngroups / split) (groups of four K blocks).
+    // Split-K: the CTAs of a cluster take the same tiles; CTA `crank` covers K blocks
+    // [crank * kblocks / split, (crank + 1) * kblocks / split), which may start or end inside a
+    // group of four K blocks (one packed scale word): the scale path loads a word for every
+    // group the range touches.
     const uint32_t crank = clustered ? cluster_ctarank() : 0u;
     const int u_first = clustered ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
     const int u_step = clustered ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
     const int total_units = args.mode == MODE_MASKED ? cum[args.groups] * args.num_n_blocks : args.num_units;
-    const int ngroups = (args.kblocks + 3) / 4;
     const int krank = split > 1 ? static_cast<int>(crank) : 0;
-    const int kb0 = 4 * (krank * ngroups / split);
-    const int kb1 = min(args.kblocks, 4 * ((krank + 1) * ngroups / split));
+    const int kb0 = krank * args.kblocks / split;
+    const int kb1 = (krank + 1) * args.kblocks / split;
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
@@ -563,8 +564,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t ph = 0;
             uint32_t issued = 0;   // stages issued in total (for the abort drain)
             bool ok = true;
-            const bool keep_b = args.mode == MODE_CONTIGUOUS || (args.mode == MODE_DENSE && args.num_m_blocks > 2);
-            const uint64_t b_policy = policy_evict_last();
             for (int u = u_first; ok && u < total_units; u += u_step) {
                 const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
                 if (t.zero) continue;
@@ -606,10 +605,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                             tma_load_3d(base + C::OFF_B + s * C::B_STAGE + j * (128 * BK), &tm_b, fb,
                                         t.nb * C::BN + j * 128, kx, gbz);
                     } else if (!pair) {
-                        // B tiles are re-read by every m-tile of their group: keep them in L2
-                        if (keep_b) tma_load_3d_hint(base + C::OFF_B + s * C::B_STAGE, &tm_b, fb, kx, t.nb * C::BN, gbz,
-                                                     b_policy);
-                        else tma_load_3d(base + C::OFF_B + s * C::B_STAGE, &tm_b, fb, kx, t.nb * C::BN, gbz);
+                        tma_load_3d(base + C::OFF_B + s * C::B_STAGE, &tm_b, fb, kx, t.nb * C::BN, gbz);
                     } else {
                         // The B map's box is half a tile; with multicast each CTA of the pair loads
                         // one half into both CTAs, otherwise each loads both halves itself.
@@ -677,8 +673,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>((acc * MH + h) * C::ACC_STRIDE);
                 for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
-                    if ((kb & 3) == 0) {
-                        // First K block of a group: copy the group's re-laid scale words from its
+                    if ((kb & 3) == 0 || kb == t.kb_begin) {
+                        // First K block of a group (or of the range): copy the group's re-laid scale words from its
                         // ring slot into this issuer's TMEM slot.  (The slot's previous MMAs are
                         // complete: the producer waited for that before loading the slot.)
                         if (!wait_fast(sfready_bar(sf_slot), (sfr_phbits >> sf_slot) & 1u, misc + 1, args.err,
@@ -755,13 +751,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
             if (t.zero) continue;
             const int ga = args.mode == MODE_MASKED ? t.g : 0;
-            for (int kb = t.kb_begin; kb < t.kb_end; kb += 4) {
+            for (int grp = t.kb_begin >> 2; grp <= (t.kb_end - 1) >> 2; ++grp) {
                 if (lane == 0) {
                     const uint32_t par = ((sfe_phbits >> sf_slot) & 1u) ^ 1u;
                     if (wait_or_abort(sfempty_bar(sf_slot), par, misc + 1, args.err, args.timeout_ns, SITE_SF_EMPTY)) {
                         const uint32_t sb = sffull_bar(sf_slot);
                         mbar_arrive_expect_tx(sb, C::TX_SF);
-                        const int kp = t.kpoff + (kb >> 2);
+                        const int kp = t.kpoff + grp;
                         tma_load_3d(base + C::OFF_SFA + sf_slot * C::SFA_BYTES, &tm_sfa, sb, t.mb * C::TM, kp, ga);
                         tma_load_3d(base + C::OFF_SFB + sf_slot * C::SFB_BYTES, &tm_sfb, sb, t.nb * C::BN, kp,
                                     args.mode == MODE_K_GROUPED ? 0 : t.gb);
