@@ -115,7 +115,6 @@ dg_status current_device(DeviceState** out) {
         const KernelConfig* const* cfgs = all_configs(&n);
         for (int i = 0; i < n; ++i)
             if ((e = cfgs[i]->prepare(st.max_smem)) != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", e);
-        if ((e = prepare_aux_kernels()) != cudaSuccess) return cuda_fail("cudaFuncSetAttribute", e);
         st.prepared = true;
     }
     *out = &st;

@@ -83,8 +83,6 @@ cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb
                            int mn_al, int gran_mn, int pdl, cudaStream_t stream);
 cudaError_t launch_pack_sf_k_grouped(const float* sf, int32_t* out, const int32_t* ks, int G, int MN, int mn_al,
                                      int kb_total, int pdl, cudaStream_t stream);
-cudaError_t prepare_quantize_kernel();
-cudaError_t prepare_aux_kernels();   // per device, once: carve-out preference of the small kernels
 cudaError_t launch_quantize_fp8_1x128(const void* x, void* q, int32_t* sf, int G, int M, int K, int pdl,
                                       cudaStream_t stream);
 

@@ -127,18 +127,6 @@ __global__ void __launch_bounds__(256) pack_sf_k_grouped_kernel(const float* __r
     out[static_cast<size_t>(w) * mn_al + r] = static_cast<int32_t>(word);
 }
 
-// The GEMM kernels run with the largest shared-memory carve-out; giving the small kernels that
-// run between them the same preference spares the SMs a carve-out change at every switch.
-cudaError_t prepare_aux_kernels() {
-    cudaError_t e = cudaFuncSetAttribute(pack_sf_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                         cudaSharedmemCarveoutMaxShared);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(pack_sf_k_grouped_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
-    if (e == cudaSuccess) e = prepare_quantize_kernel();
-    return e;
-}
-
 cudaError_t launch_pack_sf_k_grouped(const float* sf, int32_t* out, const int32_t* ks, int G, int MN, int mn_al,
                                      int kb_total, int pdl, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};

@@ -105,11 +105,6 @@ __global__ void __launch_bounds__(32 * QUANT_WARPS)
     }
 }
 
-cudaError_t prepare_quantize_kernel() {
-    return cudaFuncSetAttribute(quantize_fp8_1x128_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                cudaSharedmemCarveoutMaxShared);
-}
-
 cudaError_t launch_quantize_fp8_1x128(const void* x, void* q, int32_t* sf, int G, int M, int K, int pdl,
                                       cudaStream_t stream) {
     const int Kb = K / 128;
