@@ -101,12 +101,13 @@ struct GemmCfg {
     static constexpr int OFF_SFB = OFF_SFA + SF_SLOTS * SFA_BYTES;
     static constexpr int OFF_BAR = OFF_SFB + SF_SLOTS * SFB_BYTES;
     // full/empty per stage; tmem full/empty per accumulator; sf full/ready/empty per scale
-    // slot; split-K reduce: 4 full, 1 empty.
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 3 * SF_SLOTS + 5;
+    // slot; split-K reduce: 4 receive (one per TMEM lane quadrant), 8 slot-free (one per CTA
+    // of the cluster), 1 unit-done.
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 3 * SF_SLOTS + 13;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
     static constexpr int OFF_CUM = OFF_MISC + 16;             // masked mode: m-unit prefix sums
-    // Split-K receive buffer: one slot per other CTA of the cluster, each holding the 128 / split
-    // rows this CTA owns, BN FP32 per row (rows padded by 16 bytes).
+    // Split-K receive buffer: one slot per other CTA of the cluster, each holding the (at most
+    // 128 / split) rows this CTA owns, BN FP32 per row (rows padded by 16 bytes).
     static constexpr int RECV_ROW = BN * 4 + 16;
     static __host__ __device__ uint32_t off_recv(int extra_ints) {
         return (static_cast<uint32_t>(OFF_CUM + extra_ints * 4) + 15u) & ~15u;
@@ -422,7 +423,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     auto sfready_bar = [&](int j) { return base + C::OFF_BAR + 8u * (SFB0 + C::SF_SLOTS + j); };
     auto sffull_bar = [&](int j) { return base + C::OFF_BAR + 8u * (SFB0 + 2 * C::SF_SLOTS + j); };
     auto redfull_bar = [&](int j) { return base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + j); };
-    const uint32_t redempty_bar = base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + 4);
+    auto slotfree_bar = [&](uint32_t o) { return base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + 4 + o); };
+    const uint32_t unitdone_bar = base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + 12);
     const int split = (MH == 1 && C::EPI_COLS == 1) ? args.split : 1;
     const int pair = MH == 1 ? args.pair : 0;
     const uint32_t recv_base = base + C::off_recv(extra_smem_ints(args.mode, args.groups));
@@ -445,8 +447,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_init(sffull_bar(j), 1);
         }
         for (int j = 0; j < 4; ++j) mbar_init(redfull_bar(j), 1);
-        // every other CTA's receiving warps (two when an owner has 64 rows) free the slots once
-        mbar_init(redempty_bar, split > 1 ? static_cast<uint32_t>((split - 1) * (split == 2 ? 2 : 1)) : 1u);
+        // split-K slot handshake, per unit: CTA o's slot-free barrier here takes one arrival from
+        // CTA o and one from each epilogue warp of this CTA; the unit-done barrier one from each
+        // epilogue warp
+        for (uint32_t o = 0; o < 8; ++o) mbar_init(slotfree_bar(o), 1u + C::EPI_THREADS / 32);
+        mbar_init(unitdone_bar, C::EPI_THREADS / 32);
         misc[1] = 0u;
         fence_mbarrier_init();
     }
@@ -569,7 +574,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (t.zero) continue;
                 const int ga = args.mode == MODE_MASKED ? t.g : 0;
                 for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
-                    if (!wait_or_abort(empty_bar(s), ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_EMPTY)) {
+                    if (!wait_fast(empty_bar(s), ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_EMPTY)) {
                         ok = false;
                         break;
                     }
@@ -811,7 +816,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int N = args.N;
         int acc = 0;
         uint32_t acc_ph = 0;
-        uint32_t red_eph = 0;  // split-K: parity of the receive-slots-free barrier (sending warps)
+        uint32_t red_eph = 0;  // split-K: parity of the slot-free barriers
+        uint32_t red_dph = 0;  // split-K: parity of the unit-done barrier
         uint32_t red_fph = 0;  // split-K: parity of this warp's receive barrier (owning warps)
         for (int u = u_first; u < total_units; u += u_step) {
             if (misc[1]) break;
@@ -834,23 +840,40 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 return (static_cast<size_t>(t.g) * args.rows + row) * static_cast<size_t>(N);
             };
             if (split > 1) {
-                // Reduce-scatter of the cluster's partial accumulators: rows [o * RPO, (o+1) * RPO)
-                // of the tile belong to CTA o (RPO = 128 / split = 64, 32 or 16 rows).  Every lane
-                // whose row belongs to another CTA sends that CTA its partial row; the owner's
-                // lanes wait for the other split - 1 partials, re-read their own and add.
+                // Reduce-scatter of the cluster's partial accumulators over the tile's V valid
+                // rows (rows past the call's extent are neither sent nor summed): rows
+                // [o * RPO, min(V, (o + 1) * RPO)) belong to CTA o, RPO = ceil(V / split).  Every
+                // lane whose valid row belongs to another CTA sends that CTA its partial row; the
+                // owner's lanes wait for the other split - 1 partials, re-read their own and add.
+                // Row r stays in TMEM lane quadrant r / 32 in every CTA, so each quadrant's warp
+                // has its own receive barrier.
+                // Which warps send and receive changes with V, so the slot handshake involves every
+                // epilogue warp in every unit.  This CTA keeps one slot-free barrier per other CTA
+                // o; its phase for unit k closes when o has read all of unit k's data (one arrival
+                // from o) and every epilogue warp here has waited for the phase of unit k - 1 (one
+                // local arrival each, made after that wait, so that no phase can close before all
+                // the local warps have seen the one before it).  Before sending unit k a warp waits
+                // for the unit k - 1 phases of all of them.  After its unit, each warp arrives on
+                // the unit-done barrier and waits for the other epilogue warps there; then one
+                // thread tells every other CTA that its unit's data has been read.
                 const int row = row_of(0);
                 bool write, zero_row;
                 row_state(row, write, zero_row);
                 const size_t row_off = roff_of(row);
-                const uint32_t RPO = BM / static_cast<uint32_t>(split);
+                const uint32_t V = static_cast<uint32_t>(min(BM, max(0, m_valid - t.mb * BM)));
+                const uint32_t usplit = static_cast<uint32_t>(split);
+                const uint32_t RPO = V > 0 ? (V + usplit - 1) / usplit : 1u;
+                const uint32_t RPO_CAP = BM / usplit;                // rows of a receive slot
                 const uint32_t r_in_tile = q * 32u + lane;
-                const uint32_t owner = r_in_tile / RPO;
-                const bool recv_lane = owner == crank;
-                const uint32_t own0 = crank * RPO, own1 = own0 + RPO;          // rows this CTA owns
-                const bool warp_recv = q * 32u < own1 && q * 32u + 32u > own0;
-                const bool warp_send = !(q * 32u >= own0 && q * 32u + 32u <= own1);
-                // receiving warp index within an owner (RPO = 64: two warps per owner)
-                const uint32_t rw = (r_in_tile % RPO) / 32u;
+                const bool valid_row = r_in_tile < V;
+                const uint32_t owner = valid_row ? r_in_tile / RPO : crank;
+                const bool recv_lane = valid_row && owner == crank;
+                const bool send_lane = valid_row && owner != crank;
+                const uint32_t own0 = min(V, crank * RPO), own1 = min(V, own0 + RPO);   // rows this CTA owns
+                const uint32_t q0 = q * 32u;
+                const uint32_t ro0 = max(own0, q0), ro1 = min(own1, q0 + 32u);          // ... in this warp
+                const bool warp_recv = ro0 < ro1;
+                const bool warp_send = __any_sync(0xffffffffu, send_lane);
                 if (t.zero) {
                     if (recv_lane && write) store_zero_row(args, row_off, n0, min(N, n0 + C::BN));
                     continue;
@@ -858,21 +881,30 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (!wait_or_abort(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
                 tc_fence_after_sync();
                 const uint32_t t_row = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * C::ACC_STRIDE);
+                // the other CTAs are done with the previous unit's receive slots
+                bool slots_free = true;
+                for (uint32_t o = 0; o < usplit && slots_free; ++o)
+                    if (o != crank)
+                        slots_free = wait_cluster_or_abort(slotfree_bar(o), red_eph ^ 1u, misc + 1, args.err,
+                                                           args.timeout_ns, SITE_RED_EMPTY);
+                if (!slots_free) break;
+                red_eph ^= 1u;
+                __syncwarp();
+                if (lane == 0)
+                    for (uint32_t o = 0; o < usplit; ++o)
+                        if (o != crank) mbar_arrive(slotfree_bar(o));
                 if (warp_send) {
-                    if (!wait_cluster_or_abort(redempty_bar, red_eph ^ 1u, misc + 1, args.err, args.timeout_ns,
-                                               SITE_RED_EMPTY))
-                        break;
-                    red_eph ^= 1u;
                     const uint32_t slot = crank < owner ? crank : crank - 1u;
                     const uint32_t dst = map_to_rank(
-                        recv_base + (slot * RPO + (r_in_tile - owner * RPO)) * C::RECV_ROW, owner);
-                    const uint32_t rbar = map_to_rank(redfull_bar(static_cast<int>(rw)), owner);
+                        recv_base + (send_lane ? (slot * RPO_CAP + (r_in_tile - owner * RPO)) * C::RECV_ROW : 0u),
+                        owner);
+                    const uint32_t rbar = map_to_rank(redfull_bar(static_cast<int>(q)), owner);
 #pragma unroll 1
                     for (int c = 0; c < C::BN / 32; ++c) {
                         uint32_t r[32];
                         tmem_ld_32x32b_x32(t_row + 32u * c, r);
                         tmem_wait_ld();
-                        if (!recv_lane) {
+                        if (send_lane) {
 #pragma unroll
                             for (int j = 0; j < 8; ++j)
                                 st_async_v4(dst + 128u * c + 16u * j, r[4 * j], r[4 * j + 1], r[4 * j + 2],
@@ -881,15 +913,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                 }
                 if (warp_recv) {
-                    if (lane == (own0 > q * 32u ? own0 - q * 32u : 0u))      // first owned lane of the warp
-                        mbar_arrive_expect_tx(redfull_bar(static_cast<int>(rw)),
-                                              static_cast<uint32_t>((split - 1) * min(32u, RPO) * C::BN * 4));
+                    if (lane == ro0 - q0)      // first owned lane of the warp
+                        mbar_arrive_expect_tx(redfull_bar(static_cast<int>(q)),
+                                              (usplit - 1u) * (ro1 - ro0) * static_cast<uint32_t>(C::BN * 4));
                     __syncwarp();
-                    if (!wait_cluster_or_abort(redfull_bar(static_cast<int>(rw)), red_fph, misc + 1, args.err,
+                    if (!wait_cluster_or_abort(redfull_bar(static_cast<int>(q)), red_fph, misc + 1, args.err,
                                                args.timeout_ns, SITE_RED_FULL))
                         break;
                     red_fph ^= 1u;
-                    const uint32_t src = recv_base + (r_in_tile - own0) * C::RECV_ROW;
+                    const uint32_t src = recv_base + (recv_lane ? r_in_tile - own0 : 0u) * C::RECV_ROW;
 #pragma unroll 1
                     for (int c = 0; c < C::BN / 32; ++c) {
                         uint32_t r[32];
@@ -901,7 +933,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
                         for (int sl = 0; sl < split - 1; ++sl) {
                             const float4* p = reinterpret_cast<const float4*>(
-                                gbase + (src - base) + static_cast<uint32_t>(sl) * RPO * C::RECV_ROW + 128u * c);
+                                gbase + (src - base) + static_cast<uint32_t>(sl) * RPO_CAP * C::RECV_ROW + 128u * c);
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
                                 const float4 x = p[j];
@@ -920,15 +952,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 tc_fence_before_sync();
                 mbar_arrive(tempty_bar(acc));
-                if (warp_recv) {
-                    // The receive slots of this warp's rows may be refilled: tell every other CTA.
-                    __syncwarp();
-                    if (lane == (own0 > q * 32u ? own0 - q * 32u : 0u))
-                        for (int rk = 0; rk < split; ++rk)
-                            if (static_cast<uint32_t>(rk) != crank)
-                                mbar_arrive_remote(map_to_rank(redempty_bar, static_cast<uint32_t>(rk)));
-                }
                 if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
+                // Every epilogue warp is done with this unit's receive slots: tell every other CTA.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(unitdone_bar);
+                if (!wait_or_abort(unitdone_bar, red_dph, misc + 1, args.err, args.timeout_ns, SITE_RED_UNIT)) break;
+                red_dph ^= 1u;
+                if (warp == 2 && lane == 0)
+                    for (uint32_t rk = 0; rk < usplit; ++rk)
+                        if (rk != crank) mbar_arrive_remote(map_to_rank(slotfree_bar(crank), rk));
                 continue;
             }
             if (t.zero) {
@@ -1023,13 +1055,45 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     mbar_arrive(tempty_bar(acc));
                     if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
                     uint16_t* drow = static_cast<uint16_t*>(args.d) + row_off;
+                    // With two accumulators the stores never hold up the next tile's MMAs; they
+                    // only end the CTA's last tile, where plain stores finish sooner than the
+                    // chain of staged boxes.  Where the staging area exists they still go through
+                    // it: each 32-row x 64-byte slab is transposed in the warp's 2 KB so that one
+                    // warp store covers 8 rows x 64 contiguous bytes instead of 32 rows x 16.  The
+                    // 16-byte unit j of slab row r sits at unit j ^ ((r >> 1) & 3) of the row's 64
+                    // bytes, which keeps both the writes and the reads free of bank conflicts.
+                    int i_direct = 0;    // first piece stored row by row
+                    if (C::ACC == 2 && args.tma_store) {
+                        uint16_t* dgrp = static_cast<uint16_t*>(args.d) +
+                                         static_cast<size_t>(t.g) * args.rows * static_cast<size_t>(N);
+                        const uint32_t sw = (lane >> 1) & 3u;
+                        const uint32_t u = lane & 3u;
+#pragma unroll
+                        for (int i = 0; i + 1 < NP; i += 2) {
+                            const uint32_t* p = pk + 8 * i;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                st_shared_v4(stage_out + lane * 64u + 16u * (static_cast<uint32_t>(j) ^ sw),
+                                             make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
+                            __syncwarp();
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint32_t rr = 8u * k + (lane >> 2);
+                                const uint4 v = ld_shared_v4(stage_out + rr * 64u + 16u * (u ^ ((rr >> 1) & 3u)));
+                                const int grow = slab0 + static_cast<int>(rr);
+                                const int col = n0 + 16 * (pc0 + i) + 8 * static_cast<int>(u);
+                                if (grow < m_valid && col < N)
+                                    st_global_v4(dgrp + static_cast<size_t>(grow) * N + col, v);
+                            }
+                            __syncwarp();
+                        }
+                        i_direct = NP & ~1;
+                    }
 #pragma unroll
                     for (int i = 0; i < NP; ++i) {
+                        if (i < i_direct) continue;
                         const int col0 = n0 + 16 * (pc0 + i);
                         const uint32_t* p = pk + 8 * i;
-                        // With two accumulators the stores never hold up the next tile's MMAs; they
-                        // only end the CTA's last tile, where plain stores finish sooner than the
-                        // chain of staged boxes.
                         if (slab_tma && C::ACC == 1) {
                             put_box(col0, make_uint4(p[0], p[1], p[2], p[3]), make_uint4(p[4], p[5], p[6], p[7]));
                         } else if (write) {

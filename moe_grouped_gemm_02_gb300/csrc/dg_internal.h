@@ -12,7 +12,7 @@ enum : int { MODE_DENSE = 0, MODE_CONTIGUOUS = 1, MODE_MASKED = 2, MODE_K_GROUPE
 
 // Timeout sites recorded in the device error word (bits 8..15), DG_ERR_TIMEOUT in bits 0..7.
 enum : int { SITE_EMPTY = 1, SITE_FULL = 2, SITE_TMEM_EMPTY = 3, SITE_TMEM_FULL = 4, SITE_SF_EMPTY = 5, SITE_RED_EMPTY = 6, SITE_RED_FULL = 7,
-             SITE_SF_READY = 8, SITE_SF_FULL = 9 };
+             SITE_SF_READY = 8, SITE_SF_FULL = 9, SITE_RED_UNIT = 10 };
 
 struct GemmArgs {
     int rows;           // rows of A and D per group: M (dense), M_sum (contiguous), max_m (masked),
