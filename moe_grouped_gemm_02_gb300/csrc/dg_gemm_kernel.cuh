@@ -112,6 +112,7 @@ struct GemmCfg {
     static __host__ __device__ uint32_t off_recv(int extra_ints) {
         return (static_cast<uint32_t>(OFF_CUM + extra_ints * 4) + 15u) & ~15u;
     }
+    static_assert(128 * RECV_ROW <= OFF_SFA, "split-K staging of a whole tile fits in the operand ring");
     static __host__ __device__ uint32_t recv_bytes(int split) {
         return split > 1 ? static_cast<uint32_t>((split - 1) * (BM / split) * RECV_ROW) : 0u;
     }
@@ -893,7 +894,42 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (lane == 0)
                     for (uint32_t o = 0; o < usplit; ++o)
                         if (o != crank) mbar_arrive(slotfree_bar(o));
-                if (warp_send) {
+                // On the CTA's last unit the operand ring is idle once the accumulator is full: the
+                // partial rows are then staged there in the receive-slot layout and each run of rows
+                // bound for one owner goes out as one bulk copy (one request instead of 16 bytes per
+                // lane and instruction); the receivers count whole padded rows.
+                const bool last_unit = u + u_step >= total_units;
+                const uint32_t row_bytes =
+                    last_unit ? static_cast<uint32_t>(C::RECV_ROW) : static_cast<uint32_t>(C::BN * 4);
+                if (warp_send && last_unit) {
+                    const uint32_t stg = base + C::OFF_A + q0 * C::RECV_ROW;   // this quadrant's rows
+#pragma unroll 1
+                    for (int c = 0; c < C::BN / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                        tmem_wait_ld();
+                        if (send_lane) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                st_shared_v4(stg + lane * C::RECV_ROW + 128u * c + 16u * j,
+                                             make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]));
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint32_t v1 = min(V, q0 + 32u);
+                        for (uint32_t o = q0 / RPO; o * RPO < v1; ++o) {
+                            if (o == crank) continue;
+                            const uint32_t a = max(q0, o * RPO), b = min(v1, (o + 1u) * RPO);
+                            const uint32_t slot = crank < o ? crank : crank - 1u;
+                            bulk_copy_to_cluster(
+                                map_to_rank(recv_base + (slot * RPO_CAP + (a - o * RPO)) * C::RECV_ROW, o),
+                                stg + (a - q0) * C::RECV_ROW, (b - a) * C::RECV_ROW,
+                                map_to_rank(redfull_bar(static_cast<int>(q)), o));
+                        }
+                    }
+                } else if (warp_send) {
                     const uint32_t slot = crank < owner ? crank : crank - 1u;
                     const uint32_t dst = map_to_rank(
                         recv_base + (send_lane ? (slot * RPO_CAP + (r_in_tile - owner * RPO)) * C::RECV_ROW : 0u),
@@ -914,8 +950,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 if (warp_recv) {
                     if (lane == ro0 - q0)      // first owned lane of the warp
-                        mbar_arrive_expect_tx(redfull_bar(static_cast<int>(q)),
-                                              (usplit - 1u) * (ro1 - ro0) * static_cast<uint32_t>(C::BN * 4));
+                        mbar_arrive_expect_tx(redfull_bar(static_cast<int>(q)), (usplit - 1u) * (ro1 - ro0) * row_bytes);
                     __syncwarp();
                     if (!wait_cluster_or_abort(redfull_bar(static_cast<int>(q)), red_fph, misc + 1, args.err,
                                                args.timeout_ns, SITE_RED_FULL))
@@ -931,7 +966,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         float v[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                        for (int sl = 0; sl < split - 1; ++sl) {
+                        // (unrolled for up to 7 partials, so that the slots' loads are all in flight)
+#pragma unroll
+                        for (int sl = 0; sl < 7; ++sl) {
+                            if (sl >= split - 1) continue;
                             const float4* p = reinterpret_cast<const float4*>(
                                 gbase + (src - base) + static_cast<uint32_t>(sl) * RPO_CAP * C::RECV_ROW + 128u * c);
 #pragma unroll
@@ -953,7 +991,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 tc_fence_before_sync();
                 mbar_arrive(tempty_bar(acc));
                 if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
-                // Every epilogue warp is done with this unit's receive slots: tell every other CTA.
+                // Every epilogue warp is done with this unit's receive slots: tell every other CTA
+                // (not after the last unit, when nothing is sent again; the final cluster barrier
+                // keeps every CTA's shared memory alive until the peers' copies have landed).
+                if (last_unit) continue;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(unitdone_bar);
                 if (!wait_or_abort(unitdone_bar, red_dph, misc + 1, args.err, args.timeout_ns, SITE_RED_UNIT)) break;
