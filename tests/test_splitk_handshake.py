@@ -1,0 +1,201 @@
+"""Model check of the split-K slot handshake of the GEMM kernel's epilogue.
+
+The split-K reduce-scatter in `fp8_gemm_kernel` (csrc/dg_gemm_kernel.cuh, epilogue, `split > 1`)
+moves partial accumulator rows between the CTAs of a cluster.  Which warps send and receive
+changes from unit to unit (ownership follows the unit's valid rows V), so the kernel guards the
+single-buffered receive slots with:
+
+* per CTA and per peer CTA o, a slot-free barrier: one arrival from o once o has read all of a
+  unit's data, plus one local arrival from each epilogue warp made after its own wait;
+* before sending unit k, every epilogue warp waits for the unit k - 1 phase of all its slot-free
+  barriers;
+* per TMEM lane quadrant, a receive barrier: the receiving warp arrives with the expected byte
+  count, the peers' copies complete it;
+* after its unit, each epilogue warp arrives on a unit-done barrier and waits for all of them;
+  then one thread arrives on every peer's slot-free barrier for this CTA;
+* after a CTA's last unit nothing is sent again, so the handshake is skipped (and the last
+  unit's rows travel as whole padded rows by bulk copy).
+
+This test runs the protocol under random interleavings with the mbarrier semantics (phase,
+pending arrivals, transaction count, parity waits) and checks that no receive slot is
+overwritten while it is read, that every read sees the current unit's data, and that nothing
+deadlocks.  Two planted mistakes (no unit-done wait; no local arrivals) must be caught, which
+shows that the checker can see both failure kinds.
+"""
+import random
+
+import pytest
+
+
+class Bar:
+    """One mbarrier: phase counter, pending arrivals, transaction bytes."""
+
+    def __init__(self, count):
+        self.count = count
+        self.pending = count
+        self.tx = 0
+        self.phase = 0
+
+    def _maybe_complete(self):
+        if self.pending == 0 and self.tx == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def arrive(self, expect_tx=0):
+        self.tx += expect_tx
+        self.pending -= 1
+        assert self.pending >= 0, "more arrivals than the barrier's count"
+        self._maybe_complete()
+
+    def complete_tx(self, nbytes):
+        self.tx -= nbytes
+        self._maybe_complete()
+
+    def try_wait(self, parity):
+        # waiting on `parity` succeeds once the phase with that parity has completed
+        return (self.phase & 1) != parity
+
+
+class Deadlock(AssertionError):
+    pass
+
+
+class DataRace(AssertionError):
+    pass
+
+
+def run_protocol(split, units, seed, *, unit_done_wait=True, local_arrivals=True, bn=4, recv_row=5):
+    """units: V per unit (0 = a zero unit, skipped by every CTA).  Returns the step count."""
+    rng = random.Random(seed)
+    W, ACC = 4, 2
+    ctas = [dict(free=[Bar(1 + (W if local_arrivals else 0)) for _ in range(split)], done=Bar(W),
+                 recv=[Bar(1) for _ in range(4)], tfull=[Bar(1) for _ in range(ACC)],
+                 tempty=[Bar(W) for _ in range(ACC)], slots={}) for _ in range(split)]
+    live_units = [u for u, v in enumerate(units) if v > 0]
+    last = live_units[-1] if live_units else -1
+    last_any = len(units) - 1          # the kernel's `u + u_step >= total_units`
+
+    def mma(c):
+        X = ctas[c]
+        acc, ph = 0, 0
+        for u in live_units:
+            while not X["tempty"][acc].try_wait(ph ^ 1):
+                yield
+            for _ in range(rng.randint(0, 3)):
+                yield
+            X["tfull"][acc].arrive()
+            acc += 1
+            if acc == ACC:
+                acc, ph = 0, ph ^ 1
+
+    def epilogue(c, q):
+        X = ctas[c]
+        acc, acc_ph, free_ph, done_ph, recv_ph = 0, 0, 0, 0, 0
+        for u in live_units:
+            V = units[u]
+            last_unit = u == last_any
+            row_bytes = recv_row if last_unit else bn
+            rpo = (V + split - 1) // split
+            cap = 128 // split
+            q0 = 32 * q
+            own0 = min(V, c * rpo)
+            own1 = min(V, own0 + rpo)
+            ro0, ro1 = max(own0, q0), min(own1, q0 + 32)
+            sends = [r for r in range(q0, q0 + 32) if r < V and r // rpo != c]
+            while not X["tfull"][acc].try_wait(acc_ph):
+                yield
+            for o in range(split):
+                if o != c:
+                    while not X["free"][o].try_wait(free_ph ^ 1):
+                        yield
+            free_ph ^= 1
+            if local_arrivals:
+                for o in range(split):
+                    if o != c:
+                        X["free"][o].arrive()
+            for r in sends:                     # st.async rows, or bulk runs of rows
+                o = r // rpo
+                key = (c if c < o else c - 1, r - o * rpo)
+                assert key[1] < cap
+                prev = ctas[o]["slots"].get(key)
+                if prev is not None and prev[1] == "reading":
+                    raise DataRace(f"CTA {o} slot {key} overwritten while read (unit {u})")
+                ctas[o]["slots"][key] = (u, "written")
+                ctas[o]["recv"][q].complete_tx(row_bytes)
+                yield
+            if ro0 < ro1:
+                X["recv"][q].arrive((split - 1) * (ro1 - ro0) * row_bytes)
+                while not X["recv"][q].try_wait(recv_ph):
+                    yield
+                recv_ph ^= 1
+                keys = [(sl, r - own0) for r in range(ro0, ro1) for sl in range(split - 1)]
+                for k in keys:
+                    if X["slots"][k][0] != u:
+                        raise DataRace(f"CTA {c} read unit {X['slots'][k][0]} data in unit {u}")
+                    X["slots"][k] = (u, "reading")
+                for _ in range(rng.randint(0, 4)):
+                    yield
+                for k in keys:
+                    X["slots"][k] = (u, "read")
+            X["tempty"][acc].arrive()
+            acc += 1
+            if acc == ACC:
+                acc, acc_ph = 0, acc_ph ^ 1
+            if last_unit:
+                continue
+            X["done"].arrive()
+            if unit_done_wait:
+                while not X["done"].try_wait(done_ph):
+                    yield
+            done_ph ^= 1
+            if q == 0:
+                for rk in range(split):
+                    if rk != c:
+                        ctas[rk]["free"][c].arrive()
+                        yield
+
+    procs = []
+    for c in range(split):
+        procs.append(mma(c))
+        procs += [epilogue(c, q) for q in range(W)]
+    live = list(range(len(procs)))
+    steps = stalled = 0
+    while live:
+        i = rng.choice(live)
+        try:
+            next(procs[i])
+        except StopIteration:
+            live.remove(i)
+            stalled = 0
+            continue
+        steps += 1
+        stalled += 1
+        if stalled > 50000:
+            raise Deadlock(f"no progress (split {split}, units {units})")
+    return steps
+
+
+def _cases(n, seed0):
+    rng = random.Random(seed0)
+    for i in range(n):
+        split = rng.choice([2, 4, 8])
+        units = [rng.choice([0, 1, 2, 17, 31, 32, 33, 64, 71, 100, 127, 128, rng.randint(1, 128)])
+                 for _ in range(rng.randint(1, 7))]
+        yield i, split, units
+
+
+def test_handshake_holds_under_random_interleavings():
+    for i, split, units in _cases(120, 0):
+        run_protocol(split, units, seed=i)
+
+
+@pytest.mark.parametrize("mutation", ["no_unit_done_wait", "no_local_arrivals"])
+def test_checker_catches_planted_mistakes(mutation):
+    kw = {"unit_done_wait": False} if mutation == "no_unit_done_wait" else {"local_arrivals": False}
+    caught = 0
+    for i, split, units in _cases(120, 1):
+        try:
+            run_protocol(split, units, seed=i, **kw)
+        except (Deadlock, DataRace, AssertionError):
+            caught += 1
+    assert caught > 0, f"the checker did not see the planted mistake ({mutation})"
