@@ -21,9 +21,11 @@
 //                 blocks into a 2-3-slot ring as soon as a slot frees (a group ahead of the
 //                 operands) and re-lays them for tcgen05.cp.
 //   warps 2-5     epilogue, one output row per thread: TMEM -> registers (BF16 rows packed in
-//   (+8-11)       registers, then TMEM released) -> shared-memory boxes -> TMA bulk stores;
-//                 with MH = 2 the second set writes the second 128-row half, with MH = 1 and
-//                 one accumulator the two sets split the columns.
+//   (+8-11)       registers, then TMEM released) -> shared memory -> global: boxes written by
+//                 TMA bulk stores (one accumulator), or 32-row slabs transposed so that warp
+//                 stores are coalesced (two); with MH = 2 the second set writes the second
+//                 128-row half, with MH = 1 and one accumulator the two sets split the columns.
+//                 Split-K clusters reduce-scatter their partial rows between these warps.
 // With MH = 1 the accumulator can be double-buffered in TMEM (ACC = 2) so that the epilogue
 // of one tile overlaps the main loop of the next.  MH = 2 halves the operand bytes each SM
 // ingests per multiply-add (one B tile serves 256 rows), the limit for large GEMMs.
