@@ -402,11 +402,27 @@ __device__ __forceinline__ void store_zero_row(const GemmArgs& args, size_t row_
     for (int c = c0; c < c1; c += 32) store_row_chunk(args, row_off, c, c1, none, 32, true);
 }
 
-template <class C>
+// DENSE: the variant for dense decode-style calls (one 128-row half; dense, K-major FP8
+// operands, BF16 out, no C, no pairs), with those choices fixed at compile time so that the
+// code of the other modes is not in the kernel at all: a shorter instruction stream on every
+// role's first pass, which is a visible part of a kernel that lives for 10-20 us.
+template <class C, bool DENSE>
 __global__ void __launch_bounds__(C::THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
-                    const __grid_constant__ CUtensorMap tm_d, const GemmArgs args) {
+                    const __grid_constant__ CUtensorMap tm_d, const GemmArgs args_in) {
+    GemmArgs args = args_in;
+    if (DENSE) {
+        args.mode = MODE_DENSE;
+        args.groups = 1;
+        args.b_groups = 1;
+        args.a_mn = 0;
+        args.b_mn = 0;
+        args.b_fp4 = 0;
+        args.out_f32 = 0;
+        args.pair = 0;
+        args.c = nullptr;
+    }
     constexpr int MH = C::MH;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -1259,7 +1275,12 @@ cudaError_t launch_fp8_gemm(const CUtensorMap* maps, const GemmArgs& args, int g
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<C>, maps[0], maps[1], maps[2], maps[3], maps[4], args);
+    // (256-row tiles, the long prefill and MoE GEMMs, measured no faster with it)
+    const bool dense = C::MH == 1 && args.mode == MODE_DENSE && !args.a_mn && !args.b_mn && !args.b_fp4 &&
+                       !args.out_f32 && !args.pair && args.c == nullptr;
+    return dense ? cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<C, C::MH == 1>, maps[0], maps[1], maps[2], maps[3],
+                                      maps[4], args)
+                 : cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<C, false>, maps[0], maps[1], maps[2], maps[3], maps[4], args);
 }
 
 template <class C>
@@ -1276,7 +1297,7 @@ int max_clusters_fp8_gemm(int cluster, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel<C>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel<C, false>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -1285,7 +1306,11 @@ int max_clusters_fp8_gemm(int cluster, size_t smem) {
 
 template <class C>
 cudaError_t prepare_fp8_gemm(int max_smem) {
-    return cudaFuncSetAttribute(fp8_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    const cudaError_t e =
+        cudaFuncSetAttribute(fp8_gemm_kernel<C, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess || C::MH != 1) return e;
+    return cudaFuncSetAttribute(fp8_gemm_kernel<C, C::MH == 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                max_smem);
 }
 
 #define DG_DEFINE_CONFIG(FN, BN_, ST_, AC_, MH_)                                                     \
