@@ -402,23 +402,29 @@ __device__ __forceinline__ void store_zero_row(const GemmArgs& args, size_t row_
     for (int c = c0; c < c1; c += 32) store_row_chunk(args, row_off, c, c1, none, 32, true);
 }
 
-// DENSE: the variant for dense decode-style calls (one 128-row half; dense, K-major FP8
-// operands, BF16 out, no C, no pairs), with those choices fixed at compile time so that the
-// code of the other modes is not in the kernel at all: a shorter instruction stream on every
-// role's first pass, which is a visible part of a kernel that lives for 10-20 us.
-template <class C, bool DENSE>
+// SPEC: SPEC_ANY, or a variant for the decode-style calls (one 128-row half; K-major
+// operands, BF16 out, no C, no pairs; dense or masked; E4M3 or E2M1 B) with those choices
+// fixed at compile time, so that the code of the other modes is not in the kernel at all: a
+// shorter instruction stream on every role's first pass, which is a visible part of a kernel
+// that lives for 10-30 us.
+enum : int { SPEC_ANY = 0, SPEC_DENSE = 1, SPEC_MASKED = 2, SPEC_DENSE_FP4 = 3, SPEC_MASKED_FP4 = 4 };
+
+template <class C, int SPEC>
 __global__ void __launch_bounds__(C::THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
                     const __grid_constant__ CUtensorMap tm_d, const GemmArgs args_in) {
     GemmArgs args = args_in;
-    if (DENSE) {
-        args.mode = MODE_DENSE;
-        args.groups = 1;
-        args.b_groups = 1;
+    if (SPEC != SPEC_ANY) {
+        const bool dense = SPEC == SPEC_DENSE || SPEC == SPEC_DENSE_FP4;
+        args.mode = dense ? MODE_DENSE : MODE_MASKED;
+        if (dense) {
+            args.groups = 1;
+            args.b_groups = 1;
+        }
         args.a_mn = 0;
         args.b_mn = 0;
-        args.b_fp4 = 0;
+        args.b_fp4 = SPEC == SPEC_DENSE_FP4 || SPEC == SPEC_MASKED_FP4;
         args.out_f32 = 0;
         args.pair = 0;
         args.c = nullptr;
@@ -1275,12 +1281,23 @@ cudaError_t launch_fp8_gemm(const CUtensorMap* maps, const GemmArgs& args, int g
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    // (256-row tiles, the long prefill and MoE GEMMs, measured no faster with it)
-    const bool dense = C::MH == 1 && args.mode == MODE_DENSE && !args.a_mn && !args.b_mn && !args.b_fp4 &&
-                       !args.out_f32 && !args.pair && args.c == nullptr;
-    return dense ? cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<C, C::MH == 1>, maps[0], maps[1], maps[2], maps[3],
-                                      maps[4], args)
-                 : cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<C, false>, maps[0], maps[1], maps[2], maps[3], maps[4], args);
+    // (256-row tiles, the long prefill and MoE GEMMs, measured no faster with a variant)
+    const bool plain = C::MH == 1 && !args.a_mn && !args.b_mn && !args.out_f32 && !args.pair && args.c == nullptr;
+    const int spec = !plain                       ? SPEC_ANY
+                     : args.mode == MODE_DENSE  ? (args.b_fp4 ? SPEC_DENSE_FP4 : SPEC_DENSE)
+                     : args.mode == MODE_MASKED ? (args.b_fp4 ? SPEC_MASKED_FP4 : SPEC_MASKED)
+                                                : SPEC_ANY;
+    auto launch = [&](auto kernel) {
+        return cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], maps[2], maps[3], maps[4], args);
+    };
+    constexpr bool V = C::MH == 1;   // 256-row configurations have only the general kernel
+    switch (spec) {
+        case SPEC_DENSE: return launch(fp8_gemm_kernel<C, V ? SPEC_DENSE : SPEC_ANY>);
+        case SPEC_MASKED: return launch(fp8_gemm_kernel<C, V ? SPEC_MASKED : SPEC_ANY>);
+        case SPEC_DENSE_FP4: return launch(fp8_gemm_kernel<C, V ? SPEC_DENSE_FP4 : SPEC_ANY>);
+        case SPEC_MASKED_FP4: return launch(fp8_gemm_kernel<C, V ? SPEC_MASKED_FP4 : SPEC_ANY>);
+        default: return launch(fp8_gemm_kernel<C, SPEC_ANY>);
+    }
 }
 
 template <class C>
@@ -1297,7 +1314,7 @@ int max_clusters_fp8_gemm(int cluster, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel<C, false>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_gemm_kernel<C, SPEC_ANY>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -1306,11 +1323,16 @@ int max_clusters_fp8_gemm(int cluster, size_t smem) {
 
 template <class C>
 cudaError_t prepare_fp8_gemm(int max_smem) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(fp8_gemm_kernel<C, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    auto prep = [&](auto kernel) {
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    };
+    cudaError_t e = prep(fp8_gemm_kernel<C, SPEC_ANY>);
     if (e != cudaSuccess || C::MH != 1) return e;
-    return cudaFuncSetAttribute(fp8_gemm_kernel<C, C::MH == 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                max_smem);
+    constexpr bool V = C::MH == 1;
+    if ((e = prep(fp8_gemm_kernel<C, V ? SPEC_DENSE : SPEC_ANY>)) != cudaSuccess) return e;
+    if ((e = prep(fp8_gemm_kernel<C, V ? SPEC_MASKED : SPEC_ANY>)) != cudaSuccess) return e;
+    if ((e = prep(fp8_gemm_kernel<C, V ? SPEC_DENSE_FP4 : SPEC_ANY>)) != cudaSuccess) return e;
+    return prep(fp8_gemm_kernel<C, V ? SPEC_MASKED_FP4 : SPEC_ANY>);
 }
 
 #define DG_DEFINE_CONFIG(FN, BN_, ST_, AC_, MH_)                                                     \
