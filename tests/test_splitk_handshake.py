@@ -13,8 +13,10 @@ single-buffered receive slots with:
   count, the peers' copies complete it;
 * after its unit, each epilogue warp arrives on a unit-done barrier and waits for all of them;
   then one thread arrives on every peer's slot-free barrier for this CTA;
-* after a CTA's last unit nothing is sent again, so the handshake is skipped (and the last
-  unit's rows travel as whole padded rows by bulk copy).
+* a CTA's last unit is different: its rows travel as whole padded rows by bulk copy, every
+  epilogue warp waits (unit-done barrier) until all of them have staged their rows, then waits
+  for the receive barriers of every quadrant holding rows this CTA owns and adds and stores a
+  share of those rows; nothing is sent afterwards, so the handshake is skipped.
 
 This test runs the protocol under random interleavings with the mbarrier semantics (phase,
 pending arrivals, transaction count, parity waits) and checks that no receive slot is
@@ -90,7 +92,7 @@ def run_protocol(split, units, seed, *, unit_done_wait=True, local_arrivals=True
 
     def epilogue(c, q):
         X = ctas[c]
-        acc, acc_ph, free_ph, done_ph, recv_ph = 0, 0, 0, 0, 0
+        acc, acc_ph, free_ph, done_ph, recv_mask = 0, 0, 0, 0, 0
         for u in live_units:
             V = units[u]
             last_unit = u == last_any
@@ -123,11 +125,34 @@ def run_protocol(split, units, seed, *, unit_done_wait=True, local_arrivals=True
                 ctas[o]["slots"][key] = (u, "written")
                 ctas[o]["recv"][q].complete_tx(row_bytes)
                 yield
+            qr0 = own0 // 32
+            qr1 = (own1 - 1) // 32 + 1 if own1 > own0 else qr0
+            if last_unit:
+                if ro0 < ro1:
+                    X["recv"][q].arrive((split - 1) * (ro1 - ro0) * row_bytes)
+                X["tempty"][acc].arrive()
+                X["done"].arrive()
+                if unit_done_wait:
+                    while not X["done"].try_wait(done_ph):
+                        yield
+                done_ph ^= 1
+                for qq in range(qr0, qr1):
+                    while not X["recv"][qq].try_wait((recv_mask >> qq) & 1):
+                        yield
+                for qq in range(qr0, qr1):
+                    recv_mask ^= 1 << qq
+                # this warp's share of the owned rows, every partial of each
+                keys = [(sl, r - own0) for r in range(own0, own1) if (r - own0) % W == q for sl in range(split - 1)]
+                for k in keys:
+                    if X["slots"][k][0] != u:
+                        raise DataRace(f"CTA {c} read unit {X['slots'][k][0]} data in unit {u}")
+                for _ in range(rng.randint(0, 4)):
+                    yield
+                continue
             if ro0 < ro1:
                 X["recv"][q].arrive((split - 1) * (ro1 - ro0) * row_bytes)
-                while not X["recv"][q].try_wait(recv_ph):
+                while not X["recv"][q].try_wait((recv_mask >> q) & 1):
                     yield
-                recv_ph ^= 1
                 keys = [(sl, r - own0) for r in range(ro0, ro1) for sl in range(split - 1)]
                 for k in keys:
                     if X["slots"][k][0] != u:
@@ -137,12 +162,12 @@ def run_protocol(split, units, seed, *, unit_done_wait=True, local_arrivals=True
                     yield
                 for k in keys:
                     X["slots"][k] = (u, "read")
+            for qq in range(qr0, qr1):
+                recv_mask ^= 1 << qq
             X["tempty"][acc].arrive()
             acc += 1
             if acc == ACC:
                 acc, acc_ph = 0, acc_ph ^ 1
-            if last_unit:
-                continue
             X["done"].arrive()
             if unit_done_wait:
                 while not X["done"].try_wait(done_ph):
