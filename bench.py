@@ -488,15 +488,16 @@ def _time_launches(fn, stream, flush, reps):
 
 
 def time_hbm_streams(ws, dws, per_wl, peaks, reps: int = 5):
-    """The HBM-bound GEMMs (decode shapes, masked MoE) as they run in a model's decode step: the
-    same call back to back over distinct weight tensors (each workload's B and packed SFB
-    copied until the copies exceed twice the L2, so every launch reads its weights from HBM),
-    launched without host synchronisation, so that programmatic dependent launch overlaps each
-    launch with the one before.  Per-GEMM time = CUDA-event time of 4 passes over the copies /
-    launches; same algorithmic bytes as the bracketed number.  Adds stream_* keys to per_wl."""
+    """The HBM-bound GEMMs (decode shapes, masked MoE) as a model's decode step runs them: the
+    same call back to back over distinct weight tensors (each workload's B and packed SFB copied
+    until the copies exceed twice the L2, so every launch reads its weights from HBM), captured
+    in one CUDA graph (no host launch cost in the timing; programmatic dependent launch edges
+    let each launch overlap the one before).  Per-GEMM time = CUDA-event time of 4 graph
+    replays / launches; same algorithmic bytes as the bracketed number.  Adds stream_* keys to
+    per_wl."""
     import moe_grouped_gemm_02_gb300 as dg
-    stream = torch.cuda.current_stream()
     l2 = 129 * 1024 * 1024
+    s = torch.cuda.Stream()
     for w, dw, pw in zip(ws, dws, per_wl):
         if pw["bound"] != "hbm":
             continue
@@ -507,28 +508,36 @@ def time_hbm_streams(ws, dws, per_wl, peaks, reps: int = 5):
 
         def run(i):
             if dw.kind == "dense":
-                dg.dg_fp8_gemm_nt(dw.a, dw.sfa, bs[i], sfbs[i], dw.d)
+                dg.dg_fp8_gemm_nt(dw.a, dw.sfa, bs[i], sfbs[i], dw.d, stream=s)
             else:
-                dg.dg_m_grouped_fp8_gemm_nt_masked(dw.a, dw.sfa, bs[i], sfbs[i], dw.d, dw.idx)
+                dg.dg_m_grouped_fp8_gemm_nt_masked(dw.a, dw.sfa, bs[i], sfbs[i], dw.d, dw.idx, stream=s)
 
-        for i in range(copies):
-            run(i)
         torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            for i in range(copies):        # warm-up outside the capture (plans, attributes)
+                run(i)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(copies):
+                run(i)
         per = []
-        for _ in range(reps):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(4):
-                for i in range(copies):
-                    run(i)
-            e1.record(stream)
-            torch.cuda.synchronize()
-            per.append(e0.elapsed_time(e1) / (4 * copies))
+        with torch.cuda.stream(s):        # replays go to the current stream
+            g.replay()
+            s.synchronize()
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                for _ in range(4):
+                    g.replay()
+                e1.record(s)
+                s.synchronize()
+                per.append(e0.elapsed_time(e1) / (4 * copies))
         ms = statistics.median(per)
         gbs = w["bytes"] / (ms * 1e-3) / 1e9
         pw.update({"stream_ms": round(ms, 5), "stream_gbs": round(gbs, 1),
                    "stream_frac": round(gbs / peaks["hbm_gbs"], 4), "stream_weight_copies": copies})
-        del bs, sfbs
+        del g, bs, sfbs
     dg.dg_check_device_error()
 
 

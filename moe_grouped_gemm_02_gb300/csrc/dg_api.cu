@@ -51,7 +51,7 @@ const KernelConfig* const* all_configs(int* n) {
     static const KernelConfig* cfgs[] = {&config_bn256_s4_a1(), &config_bn224_s4_a2(),
                                          &config_bn192_s5_a2(), &config_bn128_s6_a2(), &config_bn128_s4_a2(), &config_bn64_s8_a2(),
                                          &config_bn32_s8_a2(), &config_bn224_s3_m2(), &config_bn192_s3_m2(),
-                                         &config_bn208_s3_m2()};
+                                         &config_bn208_s3_m2(), &config_bn128_s5_k2(), &config_bn192_s5_k2()};
     *n = static_cast<int>(sizeof(cfgs) / sizeof(cfgs[0]));
     return cfgs;
 }
@@ -213,6 +213,7 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                 // which the split-K reduction does not support
                 if (split > 1 && c->mh == 1 && c->acc == 1 && c->bn % 64 == 0) continue;
                 if (c->mh > 1 && (split > 1 || pair)) continue;
+                if (c->ks > 1 && pair) continue;
                 // Masked groups are filled to an unknown, typically partial, depth: 256-row tiles
                 // would mostly compute padding unless the groups are deep.
                 if (c->mh > 1 && mode == MODE_MASKED && rows < 512 && !force_cfg) continue;
@@ -234,11 +235,19 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                 // an MN-major B arrives in whole 128-column boxes
                 const double b_rows = b_mn ? 128.0 * ((c->bn + 127) / 128) : (pair ? c->bn / 2 : c->bn);
                 const double tma = 2.2 * (128.0 * c->mh + b_rows);
-                // one issuer: max(161, N/2 + 33) per MMA; two issuers (MH = 2) keep the pipe at N/2 + 33
-                const double mma = c->mh == 2 ? 8.0 * (c->bn / 2.0 + 33.0) : 4.0 * std::max(161.0, c->bn / 2.0 + 33.0);
+                // one issuer: max(161, N/2 + 33) per MMA; two issuers (MH = 2) keep the pipe at N/2 + 33;
+                // K-split issuers (KS = 2) issue two MMAs each per stage, side by side
+                const double mma = c->mh == 2   ? 8.0 * (c->bn / 2.0 + 33.0)
+                                   : c->ks == 2 ? std::max(2.0 * 161.0, 4.0 * (c->bn / 2.0 + 33.0))
+                                                : 4.0 * std::max(161.0, c->bn / 2.0 + 33.0);
                 const double t_tile = kb_per * (std::max(tma, mma) + 20.0) + 3000.0 + (split > 1 ? 1500.0 : 0.0);
                 const double cost = static_cast<double>(waves) * t_tile;
-                if (!best.cfg || cost < best_cost - 1e-9) {
+                // (within half a percent, the K-split issuers win: their stages go faster than
+                // the estimate, which sees the larger of the load and MMA times only)
+                const bool better = !best.cfg || cost < best_cost * 0.995 ||
+                                    (cost <= best_cost * 1.005 && c->ks > best.cfg->ks) ||
+                                    (cost < best_cost - 1e-9 && c->ks >= best.cfg->ks);
+                if (better) {
                     best.cfg = c;
                     best.split = split;
                     best.pair = pair;

@@ -53,22 +53,31 @@ constexpr int BM = 128;       // rows per MMA: the tcgen05 M
 constexpr int BK = 128;       // K per stage: one 128-byte swizzle row, one scale block
 constexpr int MMA_K = 32;     // K of one kind::mxf8f6f4 MMA
 constexpr uint32_t SF_WARP = 6;      // warp that re-lays scale words for tcgen05.cp
-constexpr uint32_t MMA1_WARP = 7;    // second MMA issuer (MH = 2)
+constexpr uint32_t MMA1_WARP = 7;    // second MMA issuer (MH = 2 or KS = 2)
 constexpr int DG_ERR_TIMEOUT_CODE = 6;
 
-template <int BN_, int STAGES_, int ACC_, int MH_ = 1>
+template <int BN_, int STAGES_, int ACC_, int MH_ = 1, int KS_ = 1>
 struct GemmCfg {
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
     static constexpr int ACC = ACC_;
     static constexpr int MH = MH_;                      // 128-row halves of a tile
     static constexpr int TM = BM * MH;                  // rows of a tile
+    // KS = 2: two MMA issuers split each 128-K stage (K steps 0-1 and 2-3) into the two TMEM
+    // accumulators, which the epilogue adds.  One thread issues at most one block-scaled MMA
+    // per ~161 cycles whatever its N, so for the narrow tiles of the HBM-bound shapes (N = 128,
+    // 192: 64-96 cycles of tensor work) a second issuer doubles the stage rate.  The two
+    // accumulators then serve one tile instead of alternating between tiles.
+    static constexpr int KS = KS_;
+    static constexpr int ISSUERS = MH * KS;
+    static constexpr int ACC_ROT = KS == 2 ? 1 : ACC;   // accumulator sets rotated across tiles
+    static_assert(KS == 1 || (KS == 2 && MH == 1 && ACC == 2), "K-split issuers use both accumulators of one tile");
     // warps: producer, MMA issuer, 4 epilogue, scale re-layout (MH = 1); plus a second issuer
     // and 4 more epilogue warps, one set per 128-row half (MH = 2)
     // With one 128-row half and one accumulator, the MMAs of the next tile wait for the
     // epilogue to drain TMEM: two sets of four epilogue warps then split the tile's columns.
     static constexpr int EPI_COLS = (MH == 1 && ACC_ == 1 && BN_ % 64 == 0) ? 2 : 1;
-    static constexpr int THREADS = (MH == 2 || EPI_COLS == 2) ? 384 : 224;
+    static constexpr int THREADS = (MH == 2 || EPI_COLS == 2) ? 384 : (KS == 2 ? 256 : 224);
     static constexpr int EPI_THREADS = 128 * MH * EPI_COLS;
     static_assert(MH == 1 || MH == 2, "a tile has one or two 128-row halves");
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 16 in [32, 256]");
@@ -92,7 +101,7 @@ struct GemmCfg {
     // then per slot and per issuer 4 columns of A scales and 4 per 128-row chunk of B scales.
     static constexpr int SF_COLS = 4 + 4 * SFB_CHUNKS;
     static constexpr int SF_SLOTS = MH == 2 ? 2 : 3;
-    static constexpr int TMEM_USED = ACC * MH * ACC_STRIDE + SF_SLOTS * MH * SF_COLS;
+    static constexpr int TMEM_USED = ACC * MH * ACC_STRIDE + SF_SLOTS * ISSUERS * SF_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64
                                    : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= 512, "TMEM budget exceeded");
@@ -409,6 +418,24 @@ __device__ __forceinline__ void store_zero_row(const GemmArgs& args, size_t row_
 // that lives for 10-30 us.
 enum : int { SPEC_ANY = 0, SPEC_DENSE = 1, SPEC_MASKED = 2, SPEC_DENSE_FP4 = 3, SPEC_MASKED_FP4 = 4 };
 
+// 32 (or 16) accumulator columns of this thread's row into r: with K-split issuers (KS = 2)
+// the sum of the two accumulators (the stage's two K halves), waited for; otherwise issued
+// only (the caller waits).
+template <class C, int W>
+__device__ __forceinline__ void acc_ld(uint32_t taddr, uint32_t (&r)[32]) {
+    static_assert(W == 32 || W == 16, "32 or 16 columns");
+    if (W == 32) tmem_ld_32x32b_x32(taddr, r);
+    else tmem_ld_32x32b_x16(taddr, r);
+    if (C::KS == 2) {
+        uint32_t r2[32];
+        if (W == 32) tmem_ld_32x32b_x32(taddr + C::ACC_STRIDE, r2);
+        else tmem_ld_32x32b_x16(taddr + C::ACC_STRIDE, r2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < W; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r2[i]));
+    }
+}
+
 template <class C, int SPEC>
 __global__ void __launch_bounds__(C::THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -457,7 +484,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (threadIdx.x == 0) {
         // Arrivals per phase: a stage is released by every MMA issuer (and, in pair mode, by
         // both CTAs of the pair); an accumulator is full once every issuer committed.
-        const uint32_t issuers = MH;
+        const uint32_t issuers = C::ISSUERS;
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), pair ? 2u : issuers);
@@ -668,12 +695,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
         }
-    } else if (warp == 1 || (MH == 2 && warp == MMA1_WARP)) {
+    } else if (warp == 1 || (C::ISSUERS == 2 && warp == MMA1_WARP)) {
         // ------------------------------------------------------------------ MMA issuer(s)
         // One lane per issuer, a minimal loop: the issuing thread's instruction stream is on
         // the critical path of the tensor pipe, so everything that can happen elsewhere does.
-        // Issuer h computes the tile's 128-row half h into its own accumulator; a unit whose
-        // half h is inactive still walks every barrier (issuing no MMA) to stay in step.
+        // Issuer h computes the tile's 128-row half h into its own accumulator (MH = 2), or K
+        // steps 2h and 2h + 1 of every stage into accumulator h (KS = 2); a unit whose half h is
+        // inactive still walks every barrier (issuing no MMA) to stay in step.
         if (lane == 0) {
             const uint32_t h = warp == 1 ? 0u : 1u;
             int s = 0;
@@ -688,8 +716,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t last_bar = 0, last_par = 0;
             // K-major tiles advance 32 bytes (2 descriptor units) per MMA along K; MN-major tiles
             // 32 rows of 128 bytes (256 units).
-            const uint64_t adesc0 = args.a_mn ? smem_desc_mnmajor_sw128(base + C::OFF_A + h * (BM * BK))
-                                              : smem_desc_kmajor_sw128(base + C::OFF_A + h * (BM * BK));
+            const uint32_t a_half = MH == 2 ? h * (BM * BK) : 0u;
+            const uint64_t adesc0 = args.a_mn ? smem_desc_mnmajor_sw128(base + C::OFF_A + a_half)
+                                              : smem_desc_kmajor_sw128(base + C::OFF_A + a_half);
+            constexpr int KSTEPS = BK / MMA_K / C::KS;           // K steps of a stage per issuer
+            const int k_first = C::KS == 2 ? static_cast<int>(h) * KSTEPS : 0;
             const uint64_t bdesc0 = args.b_mn ? smem_desc_mnmajor_sw128(base + C::OFF_B)
                                               : smem_desc_kmajor_sw128(base + C::OFF_B);
             const uint64_t astep = args.a_mn ? 256ull : 2ull;
@@ -699,7 +730,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int u = u_first; ok && u < total_units; u += u_step) {
                 const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
                 if (t.zero) continue;
-                const bool active = (t.hmask >> h) & 1u;
+                const bool active = MH == 2 ? ((t.hmask >> h) & 1u) != 0u : (t.hmask & 1u) != 0u;
                 if (!wait_fast(tempty_bar(acc), acc_ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_TMEM_EMPTY)) {
                     ok = false;
                     break;
@@ -718,12 +749,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         }
                         sfr_phbits ^= 1u << sf_slot;
                         tc_fence_after_sync();
-                        sfa_t = tmem_base +
-                                static_cast<uint32_t>(C::ACC * MH * C::ACC_STRIDE + (sf_slot * MH + h) * C::SF_COLS);
+                        sfa_t = tmem_base + static_cast<uint32_t>(C::ACC * MH * C::ACC_STRIDE +
+                                                                  (sf_slot * C::ISSUERS + h) * C::SF_COLS);
                         sfb_t = sfa_t + 4u;
                         if (active) {
                             tc_cp_32x128b_warpx4(sfa_t, smem_desc_sf_chunk(base + C::OFF_SFA + sf_slot * C::SFA_BYTES +
-                                                                           h * 512));
+                                                                           (MH == 2 ? h : 0u) * 512));
 #pragma unroll
                             for (int c = 0; c < C::SFB_CHUNKS; ++c)
                                 tc_cp_32x128b_warpx4(sfb_t + 4u * c, smem_desc_sf_chunk(base + C::OFF_SFB +
@@ -741,9 +772,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         const uint32_t sf_id = static_cast<uint32_t>(kb & 3);
                         const uint32_t idesc = idesc0 | (sf_id << 4) | (sf_id << 29);
 #pragma unroll
-                        for (int k = 0; k < BK / MMA_K; ++k)
+                        for (int i = 0; i < KSTEPS; ++i) {
+                            const int k = k_first + i;
                             tc_mma_mxf8f6f4(d_tmem, adesc + astep * k, bdesc + bstep * k, idesc, sfa_t, sfb_t,
-                                            (kb != t.kb_begin || k != 0) ? 1u : 0u);
+                                            (kb != t.kb_begin || i != 0) ? 1u : 0u);
+                        }
                     }
                     if (pair) tc_commit_multicast(empty_bar(s), 0x3);
                     else tc_commit(empty_bar(s));
@@ -758,7 +791,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
                 if (!ok) break;
                 tc_commit(tfull_bar(acc));
-                if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
+                if (++acc == C::ACC_ROT) { acc = 0; acc_ph ^= 1u; }
             }
             if ((!ok || misc[1]) && any_commit) {
                 // Abort: let the MMAs already issued finish before TMEM is freed.
@@ -937,7 +970,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll 1
                         for (int c = 0; c < C::BN / 32; ++c) {
                             uint32_t r[32];
-                            tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                            acc_ld<C, 32>(t_row + 32u * c, r);
                             tmem_wait_ld();
                             if (valid_row) {
 #pragma unroll
@@ -966,7 +999,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                               (usplit - 1u) * (ro1 - ro0) * static_cast<uint32_t>(C::RECV_ROW));
                     tc_fence_before_sync();
                     mbar_arrive(tempty_bar(acc));
-                    if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
+                    if (++acc == C::ACC_ROT) { acc = 0; acc_ph ^= 1u; }
                     // Every epilogue warp has staged its own rows, and the peers' rows have landed: all
                     // of them then add and store the rows this CTA owns, consecutive threads on
                     // consecutive 16-byte units of D (coalesced).  Own partial first, then the
@@ -1023,7 +1056,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll 1
                     for (int c = 0; c < C::BN / 32; ++c) {
                         uint32_t r[32];
-                        tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                        acc_ld<C, 32>(t_row + 32u * c, r);
                         tmem_wait_ld();
                         if (send_lane) {
 #pragma unroll
@@ -1045,7 +1078,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll 1
                     for (int c = 0; c < C::BN / 32; ++c) {
                         uint32_t r[32];
-                        tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                        acc_ld<C, 32>(t_row + 32u * c, r);
                         tmem_wait_ld();
                         if (!recv_lane) continue;
                         float v[32];
@@ -1076,7 +1109,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 for (uint32_t qq = qr0; qq < qr1; ++qq) red_fmask ^= 1u << qq;
                 tc_fence_before_sync();
                 mbar_arrive(tempty_bar(acc));
-                if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
+                if (++acc == C::ACC_ROT) { acc = 0; acc_ph ^= 1u; }
                 // Every epilogue warp is done with this unit's receive slots: tell every other CTA
                 // (not after the last unit, when nothing is sent again; the final cluster barrier
                 // keeps every CTA's shared memory alive until the peers' copies have landed).
@@ -1157,13 +1190,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     const int pc0 = 2 * ch_lo;                   // first piece of this thread's segment
                     uint32_t pk[NP * 8];
                     // 32 columns per TMEM load (half the round trips) where registers allow: with
-                    // 384 threads a thread has at most 168, so those kernels load 16 at a time.
-                    constexpr int LDC = C::THREADS <= 256 ? 32 : 16;
+                    // 384 threads a thread has at most 168, and K-split kernels load two
+                    // accumulators, so those load 16 at a time.
+                    constexpr int LDC = (C::THREADS <= 256 && C::KS == 1) ? 32 : 16;
                     auto load_pieces = [&](int i, auto width) {   // pieces i (and i + 1 when 32 wide)
                         uint32_t r[32];
                         const uint32_t col = t_row + 16u * static_cast<uint32_t>(pc0 + i);
-                        if (decltype(width)::value == 32) tmem_ld_32x32b_x32(col, r);
-                        else tmem_ld_32x32b_x16(col, r);
+                        acc_ld<C, decltype(width)::value>(col, r);
                         tmem_wait_ld();
 #pragma unroll
                         for (int j = 0; j < decltype(width)::value / 2; ++j)
@@ -1179,7 +1212,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     }
                     tc_fence_before_sync();
                     mbar_arrive(tempty_bar(acc));
-                    if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
+                    if (++acc == C::ACC_ROT) { acc = 0; acc_ph ^= 1u; }
                     uint16_t* drow = static_cast<uint16_t*>(args.d) + row_off;
                     // With two accumulators the stores never hold up the next tile's MMAs; they
                     // only end the CTA's last tile, where plain stores finish sooner than the
@@ -1240,8 +1273,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     uint32_t r[32];
                     const bool half_chunk = (C::BN % 32 != 0) && (c == C::BN / 32);   // 16-column tail
                     const int ncols = half_chunk ? 16 : 32;
-                    if (half_chunk) tmem_ld_32x32b_x16(t_row + 32u * c, r);
-                    else tmem_ld_32x32b_x32(t_row + 32u * c, r);
+                    if (half_chunk) acc_ld<C, 16>(t_row + 32u * c, r);
+                    else acc_ld<C, 32>(t_row + 32u * c, r);
                     float4 cv[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) cv[j] = cv_next[j];
@@ -1299,7 +1332,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         epilogue_release:
             tc_fence_before_sync();
             mbar_arrive(tempty_bar(acc));
-            if (++acc == C::ACC) { acc = 0; acc_ph ^= 1u; }
+            if (++acc == C::ACC_ROT) { acc = 0; acc_ph ^= 1u; }
         }
         if (lane == 0 && nbox > 0) bulk_wait_group_all();   // D is written before the CTA ends
         __syncwarp();
@@ -1396,12 +1429,13 @@ cudaError_t prepare_fp8_gemm(int max_smem) {
     return prep(fp8_gemm_kernel<C, V ? SPEC_MASKED_FP4 : SPEC_ANY>);
 }
 
-#define DG_DEFINE_CONFIG(FN, BN_, ST_, AC_, MH_)                                                     \
+#define DG_DEFINE_CONFIG_KS(FN, BN_, ST_, AC_, MH_, KS_)                                             \
     const KernelConfig& FN() {                                                                        \
-        using C = GemmCfg<BN_, ST_, AC_, MH_>;                                                        \
-        static const KernelConfig cfg{BN_, ST_, AC_, MH_, #FN, &C::smem_bytes, &launch_fp8_gemm<C>,  \
+        using C = GemmCfg<BN_, ST_, AC_, MH_, KS_>;                                                   \
+        static const KernelConfig cfg{BN_, ST_, AC_, MH_, KS_, #FN, &C::smem_bytes, &launch_fp8_gemm<C>, \
                                       &prepare_fp8_gemm<C>, &max_clusters_fp8_gemm<C>};               \
         return cfg;                                                                                   \
     }
+#define DG_DEFINE_CONFIG(FN, BN_, ST_, AC_, MH_) DG_DEFINE_CONFIG_KS(FN, BN_, ST_, AC_, MH_, 1)
 
 }  // namespace dg

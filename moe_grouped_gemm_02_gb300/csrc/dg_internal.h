@@ -60,6 +60,7 @@ struct KernelConfig {
     int stages;         // shared-memory pipeline depth
     int acc;            // TMEM accumulator buffers
     int mh;             // 128-row halves per tile (2: one B tile serves 256 rows)
+    int ks;             // MMA issuers splitting each stage's K steps (2: both accumulators serve one tile)
     const char* name;
     size_t (*smem_bytes)(int extra_ints, int split, int tma_store);
     GemmLaunchFn launch;
@@ -78,6 +79,8 @@ const KernelConfig& config_bn32_s8_a2();
 const KernelConfig& config_bn224_s3_m2();
 const KernelConfig& config_bn192_s3_m2();
 const KernelConfig& config_bn208_s3_m2();
+const KernelConfig& config_bn128_s5_k2();
+const KernelConfig& config_bn192_s5_k2();
 
 cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb, int Kb, int Kp,
                            int mn_al, int gran_mn, int pdl, cudaStream_t stream);

@@ -101,6 +101,7 @@ def forced(monkeypatch):
     ("config_bn256_s4_a1", None), ("config_bn224_s4_a2", None), ("config_bn192_s5_a2", None),
     ("config_bn128_s4_a2", 4), ("config_bn64_s8_a2", 8), ("config_bn32_s8_a2", 2),
     ("config_bn224_s3_m2", None), ("config_bn192_s3_m2", None), ("config_bn208_s3_m2", None),
+    ("config_bn128_s5_k2", 4), ("config_bn192_s5_k2", None),
 ])
 def test_fp8_fp4_forced_plans(forced, cfg, split):
     forced(cfg, split)

@@ -126,6 +126,8 @@ def forced(monkeypatch):
     ("config_bn192_s3_m2", None, "tt"),
     ("config_bn64_s8_a2", 8, "tt"),
     ("config_bn208_s3_m2", None, "tn"),     # 208 columns: a 16-column epilogue tail, 224-column accumulator stride
+    ("config_bn128_s5_k2", 4, "nn"),        # two issuers splitting K, two accumulators added
+    ("config_bn192_s5_k2", None, "tt"),
 ])
 def test_forced_plans_with_layouts(forced, cfg, split, layout):
     forced(cfg, split)

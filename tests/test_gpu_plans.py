@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 CONFIGS = ["config_bn256_s4_a1", "config_bn224_s4_a2", "config_bn192_s5_a2", "config_bn128_s6_a2",
            "config_bn128_s4_a2", "config_bn64_s8_a2", "config_bn32_s8_a2", "config_bn224_s3_m2",
-           "config_bn192_s3_m2", "config_bn208_s3_m2"]
+           "config_bn192_s3_m2", "config_bn208_s3_m2", "config_bn128_s5_k2", "config_bn192_s5_k2"]
 
 
 def _call_or_skip(fn, *args):
