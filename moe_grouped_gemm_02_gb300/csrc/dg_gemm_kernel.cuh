@@ -15,8 +15,9 @@
 //                 MN-major operands in boxes of 128 MN x 128 K; E2M1 B unpacked by the TMA)
 //                 into an S-stage ring.
 //   warp 1 (+7)   MMA issuers, one lane each: kind::mxf8f6f4 block-scaled MMAs (K = 32) into
-//                 TMEM; with MH = 2 each issuer owns one 128-row half of the tile, so two
-//                 instruction streams keep the tensor pipe fed.  Warp 1 also owns TMEM.
+//                 TMEM; with MH = 2 each issuer owns one 128-row half of the tile, with KS = 2
+//                 half of every stage's K steps (into its own accumulator): two instruction
+//                 streams keep the tensor pipe fed.  Warp 1 also owns TMEM.
 //   warp 6        the scale warp: loads the packed scale words of every group of four K
 //                 blocks into a 2-3-slot ring as soon as a slot frees (a group ahead of the
 //                 operands) and re-lays them for tcgen05.cp.
