@@ -487,57 +487,69 @@ def _time_launches(fn, stream, flush, reps):
     return statistics.median(ts), min(ts), max(ts)
 
 
-def time_hbm_streams(ws, dws, per_wl, peaks, reps: int = 5):
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _graph_stream_ms(call, copies: int, reps: int = 5) -> float:
+    """Per-launch ms of call(i, stream) for i in range(copies), back to back inside one CUDA
+    graph: no host launch cost in the timing, programmatic-dependent-launch edges kept (each
+    launch may overlap the one before).  Events around 4 replays."""
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for i in range(copies):           # warm-up outside the capture (plans, attributes)
+            call(i, s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(copies):
+            call(i, s)
+    per = []
+    with torch.cuda.stream(s):            # replays go to the current stream
+        g.replay()
+        s.synchronize()
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(4):
+                g.replay()
+            e1.record(s)
+            s.synchronize()
+            per.append(e0.elapsed_time(e1) / (4 * copies))
+    del g
+    return statistics.median(per)
+
+
+def _weight_copies(nbytes: int) -> int:
+    """Copies of a weight tensor that together exceed twice the L2 (2..16)."""
+    return max(2, min(16, -(-2 * L2_BYTES // nbytes)))
+
+
+def time_hbm_streams(ws, dws, per_wl, peaks):
     """The HBM-bound GEMMs (decode shapes, masked MoE) as a model's decode step runs them: the
     same call back to back over distinct weight tensors (each workload's B and packed SFB copied
     until the copies exceed twice the L2, so every launch reads its weights from HBM), captured
-    in one CUDA graph (no host launch cost in the timing; programmatic dependent launch edges
-    let each launch overlap the one before).  Per-GEMM time = CUDA-event time of 4 graph
-    replays / launches; same algorithmic bytes as the bracketed number.  Adds stream_* keys to
-    per_wl."""
+    in one CUDA graph (`_graph_stream_ms`).  Same algorithmic bytes as the bracketed number.
+    Adds stream_* keys to per_wl."""
     import moe_grouped_gemm_02_gb300 as dg
-    l2 = 129 * 1024 * 1024
-    s = torch.cuda.Stream()
     for w, dw, pw in zip(ws, dws, per_wl):
         if pw["bound"] != "hbm":
             continue
-        wbytes = dw.b.numel() * dw.b.element_size()
-        copies = max(2, min(16, -(-2 * l2 // wbytes)))
+        copies = _weight_copies(dw.b.numel() * dw.b.element_size())
         bs = [dw.b.clone() for _ in range(copies)]
         sfbs = [dw.sfb.clone() for _ in range(copies)]
 
-        def run(i):
+        def call(i, s):
             if dw.kind == "dense":
                 dg.dg_fp8_gemm_nt(dw.a, dw.sfa, bs[i], sfbs[i], dw.d, stream=s)
             else:
                 dg.dg_m_grouped_fp8_gemm_nt_masked(dw.a, dw.sfa, bs[i], sfbs[i], dw.d, dw.idx, stream=s)
 
-        torch.cuda.synchronize()
-        with torch.cuda.stream(s):
-            for i in range(copies):        # warm-up outside the capture (plans, attributes)
-                run(i)
-        s.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            for i in range(copies):
-                run(i)
-        per = []
-        with torch.cuda.stream(s):        # replays go to the current stream
-            g.replay()
-            s.synchronize()
-            for _ in range(reps):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(s)
-                for _ in range(4):
-                    g.replay()
-                e1.record(s)
-                s.synchronize()
-                per.append(e0.elapsed_time(e1) / (4 * copies))
-        ms = statistics.median(per)
+        ms = _graph_stream_ms(call, copies)
         gbs = w["bytes"] / (ms * 1e-3) / 1e9
         pw.update({"stream_ms": round(ms, 5), "stream_gbs": round(gbs, 1),
                    "stream_frac": round(gbs / peaks["hbm_gbs"], 4), "stream_weight_copies": copies})
-        del g, bs, sfbs
+        del bs, sfbs
     dg.dg_check_device_error()
 
 
@@ -564,6 +576,11 @@ def time_next_rows(dev, peaks, reps: int = 20):
         return {"row": row, "workload": name, "ms": round(ms, 5), "ms_min": round(lo, 5), "ms_max": round(hi, 5),
                 "bytes": nbytes, "gbs": round(gbs, 1), "bound": "hbm", "frac": round(gbs / peaks["hbm_gbs"], 4),
                 "peak_source": f"hbm copy (of {peaks['source']})"}
+
+    def stream_row(ms, nbytes):
+        # back to back over weight copies in one CUDA graph (see time_hbm_streams)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"stream_ms": round(ms, 5), "stream_gbs": round(gbs, 1), "stream_frac": round(gbs / peaks["hbm_gbs"], 4)}
 
     def tensor_row(row, name, ms, lo, hi, flops, nbytes):
         tf = flops / (ms * 1e-3) / 1e12
@@ -645,6 +662,11 @@ def time_next_rows(dev, peaks, reps: int = 20):
             rows.append(tensor_row(row, name, ms, lo, hi, 2.0 * M * N * K, nbytes))
         else:
             rows.append(hbm_row(row, name, ms, lo, hi, nbytes))
+            copies = _weight_copies(b.numel())
+            bs = [b.clone() for _ in range(copies)]
+            sms = _graph_stream_ms(lambda i, st: dg.dg_fp8_fp4_gemm_nt(a, sfa, bs[i], sfb, d, stream=st), copies)
+            rows[-1].update(stream_row(sms, nbytes))
+            del bs
         del a, b, sfa, sfb, d
     G, max_m, N, K = (synth.MASKED[k] for k in ("G", "max_m", "N", "K"))
     masked_m = synth.rng(0, "masked_m").integers(1, max_m + 1, size=G)
@@ -663,6 +685,12 @@ def time_next_rows(dev, peaks, reps: int = 20):
     nbytes = valid * K + G * N * K // 2 + 2 * valid * N + 4 * (sfa.numel() + sfb.numel())
     rows.append(hbm_row("FP8 x FP4 masked grouped GEMM (dg_m_grouped_fp8_fp4_gemm_nt_masked)",
                         f"fp8xfp4_masked_{G}x{max_m}x{N}x{K}", ms, lo, hi, nbytes))
+    copies = _weight_copies(b.numel())
+    bs = [b.clone() for _ in range(copies)]
+    sms = _graph_stream_ms(lambda i, st: dg.dg_m_grouped_fp8_fp4_gemm_nt_masked(a, sfa, bs[i], sfb, d, mm, stream=st),
+                           copies)
+    rows[-1].update(stream_row(sms, nbytes))
+    del bs
     return rows
 
 
