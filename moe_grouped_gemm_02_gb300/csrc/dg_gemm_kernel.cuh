@@ -907,7 +907,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 // rows (rows past the call's extent are neither sent nor summed): rows
                 // [o * RPO, min(V, (o + 1) * RPO)) belong to CTA o, RPO = ceil(V / split).  Every
                 // lane whose valid row belongs to another CTA sends that CTA its partial row; the
-                // owner's lanes wait for the other split - 1 partials, re-read their own and add.
+                // owner's lanes wait for the other split - 1 partials, re-read their own and add
+                // (on the CTA's last unit all epilogue warps share that work, see below).
                 // Row r stays in TMEM lane quadrant r / 32 in every CTA, so each quadrant's warp
                 // has its own receive barrier.
                 // Which warps send and receive changes with V, so the slot handshake involves every
