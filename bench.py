@@ -341,8 +341,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     for k in range(n_profile):
         step(pev[k])
     torch.cuda.synchronize()
-    per_kernel_ms = [statistics.mean(pev[k][i][0].elapsed_time(pev[k][i][1]) for k in range(n_profile))
-                     for i in range(len(dws))]
+    # median over the profiling steps (the first one follows a host synchronisation), with min and max
+    samples = [[pev[k][i][0].elapsed_time(pev[k][i][1]) for k in range(n_profile)] for i in range(len(dws))]
+    per_kernel_ms = [statistics.median(v) for v in samples]
     dom = int(np.argmax(per_kernel_ms))
 
     ev = [new_events() for _ in range(args.steps)]
@@ -376,12 +377,13 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     ridge = fp8_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
 
     per_wl = []
-    for w, ms in zip(ws, per_kernel_ms):
+    for w, ms, smp in zip(ws, per_kernel_ms, samples):
         tflops = w["flops"] / (ms * 1e-3) / 1e12
         gbs = w["bytes"] / (ms * 1e-3) / 1e9
         bound = "tensor" if w["flops"] / w["bytes"] > ridge else "hbm"
         frac = tflops / fp8_peak if bound == "tensor" else gbs / peaks["hbm_gbs"]
-        per_wl.append({"workload": w["name"], "ms": round(ms, 5), "tflops": round(tflops, 1),
+        per_wl.append({"workload": w["name"], "ms": round(ms, 5), "ms_min": round(min(smp), 5),
+                       "ms_max": round(max(smp), 5), "tflops": round(tflops, 1),
                        "gbs": round(gbs, 1), "bound": bound, "frac": round(frac, 4)})
     dw_ = ws[dom]
     if per_wl[dom]["bound"] == "tensor":
