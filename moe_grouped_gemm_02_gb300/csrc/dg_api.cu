@@ -187,7 +187,7 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                  int extra_ints, int b_mn, int b_fp4) {
     int n = 0;
     const KernelConfig* const* cfgs = all_configs(&n);
-    // DG_FORCE_CONFIG=<name>, DG_FORCE_SPLIT=<1|2|4>, DG_FORCE_PAIR=<0|1> pin the plan (tuning).
+    // DG_FORCE_CONFIG=<name>, DG_FORCE_SPLIT=<1|2|4|8>, DG_FORCE_PAIR=<0|1> pin the plan (tuning).
     const char* force_cfg = std::getenv("DG_FORCE_CONFIG");
     const char* force_split = std::getenv("DG_FORCE_SPLIT");
     const char* force_pair = std::getenv("DG_FORCE_PAIR");
