@@ -73,7 +73,7 @@ def test_split_k_decode_shape(split, monkeypatch):
 
 
 @pytest.mark.parametrize("cfg", ["config_bn128_s6_a2", "config_bn128_s4_a2", "config_bn64_s8_a2",
-                                 "config_bn224_s3_m2"])
+                                 "config_bn224_s3_m2", "config_bn128_s5_k2", "config_bn192_s5_k2"])
 @pytest.mark.parametrize("split", [1, 2, 4])
 def test_grouped_every_plan(cfg, split, few_sms, monkeypatch):
     monkeypatch.setenv("DG_FORCE_CONFIG", cfg)
