@@ -212,3 +212,30 @@ def test_split_k_rows_per_owner(cfg, split, few_sms, monkeypatch):
     rows = np.arange(160)[None, :] < m["masked_m"][:, None]
     assert np.array_equal(got[~rows], wantm[~rows])
     assert_within_tolerance(got[rows], wantm[rows], f"masked {cfg} split {split}")
+
+
+@pytest.mark.parametrize("cfg,split", [("config_bn128_s5_k2", 4), ("config_bn128_s4_a2", 2),
+                                       ("config_bn128_s5_k2", 2), ("config_bn64_s8_a2", 8)])
+def test_split_k_contiguous_trailing_padding(cfg, split, few_sms, monkeypatch):
+    # Whole 128-row blocks of padding after the last expert are zero units; on a few SMs each
+    # cluster walks several units and its last ones are such zero units, so the units before
+    # them take the unit-to-unit handshake path rather than the last-unit one.
+    monkeypatch.setenv("DG_FORCE_CONFIG", cfg)
+    monkeypatch.setenv("DG_FORCE_SPLIT", str(split))
+    c = synth.make_contiguous(2, 256, 2048, tokens=0, seed=9, counts=[200, 130])
+    K, pad = 2048, 3 * 128
+    a = np.concatenate([c["a"], np.full((pad, K), synth.NAN_CODE, np.uint8)])
+    sfa_f = np.concatenate([c["sfa"], np.ones((pad, c["sfa"].shape[1]), np.float32)])
+    m_idx = np.concatenate([c["m_indices"], np.full(pad, -1, np.int32)])
+    M_sum = a.shape[0]
+    csfa = oracle.pack_sf_ue8m0(sfa_f, M_sum, 1)[0]
+    csfb = oracle.pack_sf_ue8m0(c["sfb"], 256, 128)
+    d = torch.full((M_sum, 256), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
+    _call_or_skip(dg.dg_m_grouped_fp8_gemm_nt_contiguous, to_dev(a), to_dev(csfa), to_dev(c["b"]),
+                  to_dev(csfb), d, to_dev(m_idx))
+    dg.dg_check_device_error()
+    got = bits(d)
+    valid = m_idx >= 0
+    assert np.all(got[~valid] == 0)
+    want = oracle.m_grouped_fp8_gemm_nt_contiguous(a, csfa, c["b"], csfb, m_idx)
+    assert_within_tolerance(got[valid], want[valid], f"contiguous + trailing padding {cfg} split {split}")
