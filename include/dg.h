@@ -38,7 +38,7 @@
  *    accumulator).
  *  - The environment variable DG_PRINT_CONFIGS=1 prints the kernel configuration chosen
  *    for each call to stderr; DG_NUM_SMS=n caps the SMs used (as dg_set_num_sms).
- *    DG_FORCE_CONFIG / DG_FORCE_SPLIT / DG_FORCE_PAIR pin the kernel plan (tuning and tests);
+ *    DG_FORCE_CONFIG / DG_FORCE_SPLIT pin the kernel plan (tuning and tests);
  *    DG_TIMEOUT_MS sets the bound on each in-kernel barrier wait (default 4000) and
  *    DG_DEBUG_DROP_LOAD=n makes the GEMM skip its n-th load stage, so that a wait runs out:
  *    a test hook for the timeout path (dg_check_device_error then reports DG_ERR_TIMEOUT).
@@ -270,10 +270,15 @@ int dg_get_pdl(void);
 const char* dg_status_string(dg_status s);
 
 /*
- * Synchronizes `stream`, then reads and clears the device-side error word that the GEMM
- * kernels set when a barrier wait times out (about 4 s; it never happens in a correct run).
- * Returns DG_ERR_TIMEOUT if any kernel since the last check timed out, DG_ERR_CUDA if the
- * synchronization failed, DG_OK otherwise.  Not part of the pages' API: a debugging aid.
+ * Reads and clears the device-side error word that the GEMM kernels set when a barrier wait
+ * times out (about 4 s; it never happens in a correct run).  There is one word per device,
+ * shared by every stream of the process on that device, so the call first waits for all work
+ * on the current device (`stream` first, then the whole device): a timeout raised by a kernel
+ * on another stream is reported too, to whichever caller checks first.  Returns
+ * DG_ERR_TIMEOUT if any kernel on the device timed out since the last check, DG_ERR_CUDA if
+ * the synchronization failed, DG_OK otherwise.  With DG_PRINT_CONFIGS=1 the word is printed
+ * with the wait site that gave up (its bits 8..15).  Not part of the pages' API: a debugging
+ * aid.
  */
 dg_status dg_check_device_error(void* stream);
 

@@ -30,7 +30,7 @@ struct DeviceState {
     int* err_ptr = nullptr;
     int max_smem = 0;   // opt-in dynamic shared memory per block
     bool prepared = false;
-    int clusters[16][4] = {};   // co-resident clusters per configuration: split 2, 4, 8, pair (0: unknown)
+    int clusters[16][3] = {};   // co-resident clusters per configuration: split 2, 4, 8 (0: unknown)
 };
 
 std::mutex g_mu;
@@ -157,18 +157,16 @@ bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, uint64_t elem_bytes, cons
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Plan choice: a kernel configuration, a split-K factor, and whether CTA pairs share B tiles by
-// multicast.  The estimate, from GB300 measurements, is waves * (K blocks per CTA * t_kb + t_tile
-// + t_reduce).  Per K block, an SM's TMA moves about one 128-byte row per 2.2 cycles (A: 128
-// rows, B: BN rows, or BN / 2 in pair mode) and a 128 x N x 32 MMA costs max(161, N / 2 + 33)
-// cycles (four per K block); t_kb is the larger.  A tile costs about 3000 cycles of fixed
-// work (pipeline fill, epilogue), a split-K reduction about 1500.  Waves count tiles per
-// co-resident CTA, cluster or pair.
+// Plan choice: a kernel configuration and a split-K factor.  The estimate, from GB300
+// measurements, is waves * (K blocks per CTA * t_kb + t_tile + t_reduce).  Per K block, an SM's
+// TMA moves about one 128-byte row per 2.2 cycles (A: 128 rows per half, B: BN rows) and a
+// 128 x N x 32 MMA costs max(161, N / 2 + 33) cycles (four per K block); t_kb is the larger.
+// A tile costs about 3000 cycles of fixed work (pipeline fill, epilogue), a split-K reduction
+// about 1500.  Waves count tiles per co-resident CTA or cluster.
 struct Plan {
     const KernelConfig* cfg = nullptr;
     int split = 1;
-    int pair = 0;
-    int capacity = 0;   // co-resident CTAs (plain) or clusters (split > 1, pair)
+    int capacity = 0;   // co-resident CTAs (plain) or clusters (split > 1)
     int tma_store = 0;  // room for the epilogue's output staging buffers
 };
 
@@ -187,74 +185,61 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                  int extra_ints, int b_mn, int b_fp4) {
     int n = 0;
     const KernelConfig* const* cfgs = all_configs(&n);
-    // DG_FORCE_CONFIG=<name>, DG_FORCE_SPLIT=<1|2|4|8>, DG_FORCE_PAIR=<0|1> pin the plan (tuning).
+    // DG_FORCE_CONFIG=<name>, DG_FORCE_SPLIT=<1|2|4|8> pin the plan (tuning).
     const char* force_cfg = std::getenv("DG_FORCE_CONFIG");
     const char* force_split = std::getenv("DG_FORCE_SPLIT");
-    const char* force_pair = std::getenv("DG_FORCE_PAIR");
     const int fsplit = force_split ? std::atoi(force_split) : 0;
-    const int fpair = force_pair ? std::atoi(force_pair) : -1;
     Plan best;
     double best_cost = 0;
     for (int i = 0; i < n; ++i) {
         const KernelConfig* c = cfgs[i];
         if (force_cfg && std::strcmp(force_cfg, c->name) != 0) continue;
-        for (int pair = 0; pair <= 1; ++pair) {
-            // Pair multicast measured no faster on GB300 (each SM still ingests the whole B
-            // tile), so it is used only when forced.
-            if (fpair >= 0 ? pair != fpair : pair != 0) continue;
-            for (int split : {1, 2, 4, 8}) {
-                if (fsplit && split != fsplit) continue;
-                if (pair && split > 1) continue;
-                // MN-major B is loaded in boxes of 128 columns; K-grouped tiles have per-group K.
-                if (b_mn && c->bn % 128 != 0 && c->mh != 2) continue;
-                if ((b_mn || b_fp4 || mode == MODE_K_GROUPED) && pair) continue;
-                if (mode == MODE_K_GROUPED && split > 1) continue;
-                // one 128-row half with one accumulator: the epilogue warps split the columns,
-                // which the split-K reduction does not support
-                if (split > 1 && c->mh == 1 && c->acc == 1 && c->bn % 64 == 0) continue;
-                if (c->mh > 1 && (split > 1 || pair)) continue;
-                if (c->ks > 1 && pair) continue;
-                // Masked groups are filled to an unknown, typically partial, depth: 256-row tiles
-                // would mostly compute padding unless the groups are deep.
-                if (c->mh > 1 && mode == MODE_MASKED && rows < 512 && !force_cfg) continue;
-                if (split > 1 && (kblocks < split || c->bn % 32 != 0)) continue;
-                if (c->smem_bytes(extra_ints, split, 0) > static_cast<size_t>(st.max_smem)) continue;
-                const int tma_store = split == 1 && c->smem_bytes(extra_ints, 1, 1) <= static_cast<size_t>(st.max_smem);
-                int cap = sms;
-                if (split > 1)
-                    cap = std::min(cluster_capacity(st, i, c, split, split == 2 ? 0 : (split == 4 ? 1 : 2), split,
-                                                    extra_ints),
-                                   sms / split);
-                else if (pair)
-                    cap = std::min(cluster_capacity(st, i, c, 2, 3, 1, extra_ints), sms / 2);
-                if (cap <= 0) continue;
-                const long long m_units = (pair || c->mh == 2) ? (m_blocks_total + 1) / 2 : m_blocks_total;
-                const long long tiles = m_units * ((N + c->bn - 1) / c->bn);
-                const long long waves = (tiles + cap - 1) / cap;
-                const double kb_per = static_cast<double>((kblocks + split - 1) / split);
-                // an MN-major B arrives in whole 128-column boxes
-                const double b_rows = b_mn ? 128.0 * ((c->bn + 127) / 128) : (pair ? c->bn / 2 : c->bn);
-                const double tma = 2.2 * (128.0 * c->mh + b_rows);
-                // one issuer: max(161, N/2 + 33) per MMA; two issuers (MH = 2) keep the pipe at N/2 + 33;
-                // K-split issuers (KS = 2) issue two MMAs each per stage, side by side
-                const double mma = c->mh == 2   ? 8.0 * (c->bn / 2.0 + 33.0)
-                                   : c->ks == 2 ? std::max(2.0 * 161.0, 4.0 * (c->bn / 2.0 + 33.0))
-                                                : 4.0 * std::max(161.0, c->bn / 2.0 + 33.0);
-                const double t_tile = kb_per * (std::max(tma, mma) + 20.0) + 3000.0 + (split > 1 ? 1500.0 : 0.0);
-                const double cost = static_cast<double>(waves) * t_tile;
-                // (within half a percent, the K-split issuers win: their stages go faster than
-                // the estimate, which sees the larger of the load and MMA times only)
-                const bool better = !best.cfg || cost < best_cost * 0.995 ||
-                                    (cost <= best_cost * 1.005 && c->ks > best.cfg->ks) ||
-                                    (cost < best_cost - 1e-9 && c->ks >= best.cfg->ks);
-                if (better) {
-                    best.cfg = c;
-                    best.split = split;
-                    best.pair = pair;
-                    best.capacity = cap;
-                    best.tma_store = tma_store;
-                    best_cost = cost;
-                }
+        for (int split : {1, 2, 4, 8}) {
+            if (fsplit && split != fsplit) continue;
+            // MN-major B is loaded in boxes of 128 columns; K-grouped tiles have per-group K.
+            if (b_mn && c->bn % 128 != 0 && c->mh != 2) continue;
+            if (mode == MODE_K_GROUPED && split > 1) continue;
+            // one 128-row half with one accumulator: the epilogue warps split the columns,
+            // which the split-K reduction does not support
+            if (split > 1 && c->mh == 1 && c->acc == 1 && c->bn % 64 == 0) continue;
+            if (c->mh > 1 && split > 1) continue;
+            // Masked groups are filled to an unknown, typically partial, depth: 256-row tiles
+            // would mostly compute padding unless the groups are deep.
+            if (c->mh > 1 && mode == MODE_MASKED && rows < 512 && !force_cfg) continue;
+            if (split > 1 && (kblocks < split || c->bn % 32 != 0)) continue;
+            if (c->smem_bytes(extra_ints, split, 0) > static_cast<size_t>(st.max_smem)) continue;
+            const int tma_store = split == 1 && c->smem_bytes(extra_ints, 1, 1) <= static_cast<size_t>(st.max_smem);
+            int cap = sms;
+            if (split > 1)
+                cap = std::min(cluster_capacity(st, i, c, split, split == 2 ? 0 : (split == 4 ? 1 : 2), split,
+                                                extra_ints),
+                               sms / split);
+            if (cap <= 0) continue;
+            const long long m_units = c->mh == 2 ? (m_blocks_total + 1) / 2 : m_blocks_total;
+            const long long tiles = m_units * ((N + c->bn - 1) / c->bn);
+            const long long waves = (tiles + cap - 1) / cap;
+            const double kb_per = static_cast<double>((kblocks + split - 1) / split);
+            // an MN-major B arrives in whole 128-column boxes
+            const double b_rows = b_mn ? 128.0 * ((c->bn + 127) / 128) : c->bn;
+            const double tma = 2.2 * (128.0 * c->mh + b_rows);
+            // one issuer: max(161, N/2 + 33) per MMA; two issuers (MH = 2) keep the pipe at N/2 + 33;
+            // K-split issuers (KS = 2) issue two MMAs each per stage, side by side
+            const double mma = c->mh == 2   ? 8.0 * (c->bn / 2.0 + 33.0)
+                               : c->ks == 2 ? std::max(2.0 * 161.0, 4.0 * (c->bn / 2.0 + 33.0))
+                                            : 4.0 * std::max(161.0, c->bn / 2.0 + 33.0);
+            const double t_tile = kb_per * (std::max(tma, mma) + 20.0) + 3000.0 + (split > 1 ? 1500.0 : 0.0);
+            const double cost = static_cast<double>(waves) * t_tile;
+            // (within half a percent, the K-split issuers win: their stages go faster than
+            // the estimate, which sees the larger of the load and MMA times only)
+            const bool better = !best.cfg || cost < best_cost * 0.995 ||
+                                (cost <= best_cost * 1.005 && c->ks > best.cfg->ks) ||
+                                (cost < best_cost - 1e-9 && c->ks >= best.cfg->ks);
+            if (better) {
+                best.cfg = c;
+                best.split = split;
+                best.capacity = cap;
+                best.tma_store = tma_store;
+                best_cost = cost;
             }
         }
     }
@@ -382,7 +367,7 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
         ok = ok && (call.b_mn ? encode_3d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, N, Km, bz, 128, 128,
                                           CU_TENSOR_MAP_SWIZZLE_128B)
                               : encode_3d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, Km, N, bz, 128,
-                                          plan.pair ? cfg->bn / 2 : cfg->bn, CU_TENSOR_MAP_SWIZZLE_128B));
+                                          cfg->bn, CU_TENSOR_MAP_SWIZZLE_128B));
     }
     ok = ok && encode_3d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_INT32, 4, sfa, al4(rows), kp_rows, a_groups,
                          128 * cfg->mh, 1, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -430,8 +415,7 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     args.pdl = pdl_enabled();
     args.tma_store = plan.tma_store;
     if (const char* t = std::getenv("DG_DEBUG_DROP_LOAD")) args.debug_drop_stage = std::atoi(t);
-    args.pair = plan.pair;
-    args.num_m_units = (plan.pair || cfg->mh == 2) ? (m_blocks + 1) / 2 : m_blocks;
+    args.num_m_units = cfg->mh == 2 ? (m_blocks + 1) / 2 : m_blocks;
     long long units_upper = static_cast<long long>(args.num_m_units) * groups * args.num_n_blocks;
     // 256-row tiles of the contiguous layout get two passes (one per expert when they straddle).
     const long long passes = (cfg->mh == 2 && mode == MODE_CONTIGUOUS) ? 2 : 1;
@@ -445,13 +429,13 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     args.split = plan.split;
     // Persistent grid: one CTA (or one cluster) per co-resident slot.
     const long long slots = units_upper < plan.capacity ? units_upper : plan.capacity;
-    const int grid = static_cast<int>(slots) * (plan.split > 1 ? plan.split : (plan.pair ? 2 : 1));
+    const int grid = static_cast<int>(slots) * plan.split;
     if (env_flag("DG_PRINT_CONFIGS"))
         std::fprintf(stderr,
                      "[dg] mode=%d groups=%d rows=%d N=%d K=%d a_mn=%d b_mn=%d f32=%d -> %s (BN=%d stages=%d acc=%d "
-                     "mh=%d) split=%d pair=%d grid=%d raster_n=%d\n",
+                     "mh=%d) split=%d grid=%d raster_n=%d\n",
                      mode, groups, rows, N, K, call.a_mn, call.b_mn, call.out_f32, cfg->name, cfg->bn, cfg->stages,
-                     cfg->acc, cfg->mh, plan.split, plan.pair, grid, args.raster_n);
+                     cfg->acc, cfg->mh, plan.split, grid, args.raster_n);
     if (grid <= 0) return DG_OK;
     const cudaError_t e = cfg->launch(maps, args, grid, cs);
     return e == cudaSuccess ? DG_OK : cuda_fail("kernel launch", e);
@@ -726,13 +710,17 @@ dg_status dg_check_device_error(void* stream) {
     DeviceState* st = nullptr;
     const dg_status s = current_device(&st);
     if (s != DG_OK) return s;
+    // The word is shared by every stream on the device: wait for all of them.
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DG_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return DG_ERR_CUDA;
     int word = 0;
     if (cudaMemcpy(&word, st->err_ptr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DG_ERR_CUDA;
     if (word != 0) {
         const int zero = 0;
         if (cudaMemcpy(st->err_ptr, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return DG_ERR_CUDA;
-        if (env_flag("DG_PRINT_CONFIGS")) std::fprintf(stderr, "[dg] device error word 0x%x\n", word);
+        if (env_flag("DG_PRINT_CONFIGS"))
+            std::fprintf(stderr, "[dg] device error word 0x%x: status %d at wait site %d\n", word, word & 0xff,
+                         (word >> 8) & 0xff);
         return DG_ERR_TIMEOUT;
     }
     return DG_OK;

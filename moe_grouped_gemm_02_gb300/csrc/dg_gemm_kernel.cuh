@@ -35,8 +35,8 @@
 // first row from m_indices, padding rows are written as +0.0); M-grouped masked (the
 // per-group valid-row counts are read on the device, only valid rows are computed and
 // written); K-grouped (per-group K ranges read on the device, MN-major operands, FP32 out).
-// Options (runtime, MH = 1): split-K over a cluster of 2, 4 or 8 CTAs reduced through
-// distributed shared memory; CTA pairs sharing B tiles by TMA multicast.
+// Option (runtime, MH = 1): split-K over a cluster of 2, 4 or 8 CTAs reduced through
+// distributed shared memory.  Every CTA loads its own operand tiles.
 //
 // Every barrier wait is bounded (GemmArgs::timeout_ns).  On timeout the kernel records the
 // site in the device error word, raises a CTA-wide abort flag, lets every role leave its
@@ -147,7 +147,6 @@ struct Unit {
     int mb;         // m-tile within the group (tile rows mb*128*MH .. +128*MH)
     int nb;         // n-block
     bool zero;      // nothing to compute (padding or an empty pass): write zeros / skip
-    bool mc;        // pair mode: the two CTAs of the pair share B, loaded by multicast
     uint32_t hmask; // MH = 2: the 128-row halves computed in this unit
     int kb_begin;   // K blocks [kb_begin, kb_end) of this unit (the CTA's split-K share, or
     int kb_end;     //   the group's K blocks in K-grouped mode)
@@ -158,17 +157,12 @@ struct Unit {
 // Unit u of the schedule.
 //  * Plain: m-tile x n-block, in raster bands of raster_n n-blocks (dense, contiguous), or
 //    per group over the device-side prefix sums (masked).
-//  * Pair mode (MH = 1): a unit is an m-block pair; CTA `crank` takes m-block 2*pair+crank.
-//    Both CTAs run the main loop unless both blocks are padding, and share B by multicast
-//    unless the blocks belong to different experts.
 //  * MH = 2, contiguous: each m-tile has two passes; the units of pass 1 follow all those of
 //    pass 0.  If a tile's two halves belong to one expert, pass 0 computes both and pass 1 is
 //    empty; if they belong to two experts, pass h computes half h with that half's expert.
 template <int MH>
-__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cum, int u, uint32_t crank, int kb0,
-                                            int kb1) {
+__device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cum, int u, int kb0, int kb1) {
     Unit t;
-    t.mc = a.pair != 0;
     t.hmask = MH == 2 ? 3u : 1u;
     t.kb_begin = kb0;
     t.kb_end = kb1;
@@ -221,7 +215,6 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cum, i
         t.mb = local % mbs;      // m-units of one B tile run side by side
         t.nb = local / mbs;
         t.zero = false;
-        if (a.pair) t.mb = 2 * t.mb + static_cast<int>(crank);
     } else {
         const int per_band = a.num_m_units * a.raster_n;
         const int band = u / per_band;
@@ -253,22 +246,11 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cum, i
                     t.gb = pass == 0 ? e0 : e1;    // two experts: one half per pass
                     t.hmask = 1u << pass;
                 }
-            } else if (a.pair) {
-                const int mu = t.mb;
-                t.mb = 2 * mu + static_cast<int>(crank);
-                const int e_own = expert(t.mb), e_peer = expert(2 * mu + 1 - static_cast<int>(crank));
-                t.zero = e_own < 0 && e_peer < 0;
-                const int gb_own = e_own >= 0 ? e_own : e_peer;
-                const int gb_peer = e_peer >= 0 ? e_peer : e_own;
-                t.gb = t.zero ? 0 : gb_own;
-                t.mc = gb_own == gb_peer;
             } else {
                 const int e = expert(t.mb);
                 t.zero = e < 0;
                 t.gb = t.zero ? 0 : e;
             }
-        } else if (a.pair) {
-            t.mb = 2 * t.mb + static_cast<int>(crank);
         }
     }
     return t;
@@ -413,7 +395,7 @@ __device__ __forceinline__ void store_zero_row(const GemmArgs& args, size_t row_
 }
 
 // SPEC: SPEC_ANY, or a variant for the decode-style calls (one 128-row half; K-major
-// operands, BF16 out, no C, no pairs; dense or masked; E4M3 or E2M1 B) with those choices
+// operands, BF16 out, no C; dense or masked; E4M3 or E2M1 B) with those choices
 // fixed at compile time, so that the code of the other modes is not in the kernel at all: a
 // shorter instruction stream on every role's first pass, which is a visible part of a kernel
 // that lives for 10-30 us.
@@ -454,7 +436,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         args.b_mn = 0;
         args.b_fp4 = SPEC == SPEC_DENSE_FP4 || SPEC == SPEC_MASKED_FP4;
         args.out_f32 = 0;
-        args.pair = 0;
         args.c = nullptr;
     }
     constexpr int MH = C::MH;
@@ -479,16 +460,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     auto slotfree_bar = [&](uint32_t o) { return base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + 4 + o); };
     const uint32_t unitdone_bar = base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + 12);
     const int split = (MH == 1 && C::EPI_COLS == 1) ? args.split : 1;
-    const int pair = MH == 1 ? args.pair : 0;
     const uint32_t recv_base = base + C::off_recv(extra_smem_ints(args.mode, args.groups));
 
     if (threadIdx.x == 0) {
-        // Arrivals per phase: a stage is released by every MMA issuer (and, in pair mode, by
-        // both CTAs of the pair); an accumulator is full once every issuer committed.
+        // Arrivals per phase: a stage is released by every MMA issuer; an accumulator is full
+        // once every issuer committed.
         const uint32_t issuers = C::ISSUERS;
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), pair ? 2u : issuers);
+            mbar_init(empty_bar(s), issuers);
         }
         for (int a = 0; a < C::ACC; ++a) {
             mbar_init(tfull_bar(a), issuers);
@@ -524,16 +504,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     griddep_wait();
     griddep_launch_dependents();
     if (args.mode == MODE_MASKED && warp == 2) {
-        // cum[g] = sum over g' < g of the m-units of group g' (128*MH-row tiles, or pairs of
-        // 128-row blocks): each lane sums a contiguous run of groups, then an exclusive warp
+        // cum[g] = sum over g' < g of the m-units of group g' (128*MH-row tiles): each lane sums a contiguous run of groups, then an exclusive warp
         // scan over the runs.
         const int G = args.groups;
         const int per = (G + 31) / 32;
         const int g0 = min(G, static_cast<int>(lane) * per), g1 = min(G, g0 + per);
         auto units_of = [&](int g) {
             const int m = min(max(__ldg(args.masked_m + g), 0), args.rows);
-            const int blocks = (m + C::TM - 1) / C::TM;
-            return pair ? (blocks + 1) / 2 : blocks;
+            return (m + C::TM - 1) / C::TM;
         };
         int run = 0;
         for (int g = g0; g < g1; ++g) run += units_of(g);
@@ -585,13 +563,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
     }
     tc_fence_before_sync();
-    const bool clustered = split > 1 || pair;
+    const bool clustered = split > 1;
     // The producer needs nothing another warp prepares (except the masked and K-grouped
-    // prefix sums),
-    // and outside pair mode it only writes its own CTA's shared memory: it arrives without
+    // prefix sums), and it only writes its own CTA's shared memory: it arrives without
     // waiting and starts loading at once.  Everyone else waits for the barrier initialisation,
     // the TMEM address and, in a cluster, for every peer to be initialised.
-    const bool early_producer = warp == 0 && args.mode != MODE_MASKED && args.mode != MODE_K_GROUPED && !pair;
+    const bool early_producer = warp == 0 && args.mode != MODE_MASKED && args.mode != MODE_K_GROUPED;
     if (clustered) {
         // The early producer's warp holds thread 0, which initialised the barriers and published
         // them with fence.mbarrier_init: its arrival needs no release (measured 0.3 us sooner
@@ -627,7 +604,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t issued = 0;   // stages issued in total (for the abort drain)
             bool ok = true;
             for (int u = u_first; ok && u < total_units; u += u_step) {
-                const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
+                const Unit t = decode_unit<MH>(args, cum, u, kb0, kb1);
                 if (t.zero) continue;
                 const int ga = args.mode == MODE_MASKED ? t.g : 0;
                 for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
@@ -666,20 +643,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         for (int j = 0; j < C::B_BOXES; ++j)
                             tma_load_3d(base + C::OFF_B + s * C::B_STAGE + j * (128 * BK), &tm_b, fb,
                                         t.nb * C::BN + j * 128, kx, gbz);
-                    } else if (!pair) {
-                        tma_load_3d(base + C::OFF_B + s * C::B_STAGE, &tm_b, fb, kx, t.nb * C::BN, gbz);
                     } else {
-                        // The B map's box is half a tile; with multicast each CTA of the pair loads
-                        // one half into both CTAs, otherwise each loads both halves itself.
-                        constexpr int H = C::BN / 2;
-                        const uint32_t dst = base + C::OFF_B + s * C::B_STAGE;
-                        if (t.mc) {
-                            tma_load_3d_multicast(dst + crank * (H * BK), &tm_b, fb, kb * BK,
-                                                  t.nb * C::BN + static_cast<int>(crank) * H, t.gb, 0x3);
-                        } else {
-                            tma_load_3d(dst, &tm_b, fb, kb * BK, t.nb * C::BN, t.gb);
-                            tma_load_3d(dst + H * BK, &tm_b, fb, kb * BK, t.nb * C::BN + H, t.gb);
-                        }
+                        tma_load_3d(base + C::OFF_B + s * C::B_STAGE, &tm_b, fb, kx, t.nb * C::BN, gbz);
                     }
                     ++issued;
                     if (++s == C::STAGES) { s = 0; ph ^= 1u; }
@@ -729,7 +694,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint32_t idesc0 = idesc_mxf8_e4m3(BM, C::BN, 0) | idesc_mn_major(args.a_mn, args.b_mn) |
                                     (args.b_fp4 ? idesc_b_e2m1() : 0u);
             for (int u = u_first; ok && u < total_units; u += u_step) {
-                const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
+                const Unit t = decode_unit<MH>(args, cum, u, kb0, kb1);
                 if (t.zero) continue;
                 const bool active = MH == 2 ? ((t.hmask >> h) & 1u) != 0u : (t.hmask & 1u) != 0u;
                 if (!wait_fast(tempty_bar(acc), acc_ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_TMEM_EMPTY)) {
@@ -779,8 +744,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                             (kb != t.kb_begin || i != 0) ? 1u : 0u);
                         }
                     }
-                    if (pair) tc_commit_multicast(empty_bar(s), 0x3);
-                    else tc_commit(empty_bar(s));
+                    tc_commit(empty_bar(s));
                     if ((kb & 3) == 3 || kb == t.kb_end - 1) {
                         tc_commit(sfempty_bar(sf_slot));
                         if (++sf_slot == C::SF_SLOTS) sf_slot = 0;
@@ -816,7 +780,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         uint32_t sf_last_par = 0;
         bool ok = true;
         for (int u = u_first; ok && u < total_units; u += u_step) {
-            const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
+            const Unit t = decode_unit<MH>(args, cum, u, kb0, kb1);
             if (t.zero) continue;
             const int ga = args.mode == MODE_MASKED ? t.g : 0;
             for (int grp = t.kb_begin >> 2; grp <= (t.kb_end - 1) >> 2; ++grp) {
@@ -884,7 +848,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         uint32_t red_fmask = 0;  // split-K: parities of the four receive barriers
         for (int u = u_first; u < total_units; u += u_step) {
             if (misc[1]) break;
-            const Unit t = decode_unit<MH>(args, cum, u, crank, kb0, kb1);
+            const Unit t = decode_unit<MH>(args, cum, u, kb0, kb1);
             if (t.zero && t.hmask == 0u) continue;     // an empty pass: nothing to write
             const int n0 = t.nb * C::BN;
             const int m_valid = args.mode == MODE_MASKED ? min(max(__ldg(args.masked_m + t.g), 0), args.rows)
@@ -1355,7 +1319,7 @@ template <class C>
 cudaError_t launch_fp8_gemm(const CUtensorMap* maps, const GemmArgs& args, int grid, cudaStream_t stream) {
     const int extra = extra_smem_ints(args.mode, args.groups);
     const size_t smem = C::smem_bytes(extra, args.split, args.tma_store);
-    const int cluster = args.split > 1 ? args.split : (args.pair ? 2 : 1);
+    const int cluster = args.split > 1 ? args.split : 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(C::THREADS, 1, 1);
@@ -1378,7 +1342,7 @@ cudaError_t launch_fp8_gemm(const CUtensorMap* maps, const GemmArgs& args, int g
     cfg.attrs = attr;
     cfg.numAttrs = n;
     // (256-row tiles, the long prefill and MoE GEMMs, measured no faster with a variant)
-    const bool plain = C::MH == 1 && !args.a_mn && !args.b_mn && !args.out_f32 && !args.pair && args.c == nullptr;
+    const bool plain = C::MH == 1 && !args.a_mn && !args.b_mn && !args.out_f32 && args.c == nullptr;
     const int spec = !plain                       ? SPEC_ANY
                      : args.mode == MODE_DENSE  ? (args.b_fp4 ? SPEC_DENSE_FP4 : SPEC_DENSE)
                      : args.mode == MODE_MASKED ? (args.b_fp4 ? SPEC_MASKED_FP4 : SPEC_MASKED)

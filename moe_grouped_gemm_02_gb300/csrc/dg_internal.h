@@ -26,9 +26,8 @@ struct GemmArgs {
     int kblocks;        // K / 128
     int raster_n;       // n-blocks per raster band (dense and contiguous)
     int num_units;      // tiles to compute (dense and contiguous); masked counts on the device
-    int split;          // CTAs (a thread-block cluster) sharing one tile's K range: 1, 2 or 4
-    int pair;           // 1: clusters of 2 CTAs on adjacent m-blocks share each B tile by TMA multicast
-    int num_m_units;    // m-blocks, or m-block pairs when pair == 1 (dense and contiguous)
+    int split;          // CTAs (a thread-block cluster) sharing one tile's K range: 1, 2, 4 or 8
+    int num_m_units;    // m-tiles: 128-row blocks, or 256-row pairs of them when MH = 2
     int a_mn;           // 1: A is stored MN-major ([K, rows], rows contiguous)
     int b_mn;           // 1: B is stored MN-major ([K, N], N contiguous)
     int out_f32;        // 1: D is FP32; 0: BF16

@@ -188,17 +188,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// Same, multicast: the box lands at the same shared-memory offset in every CTA of the cluster
-// named in cta_mask, and each destination CTA's mbarrier (same offset) counts the bytes.
-__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
-                                                      int32_t y, int32_t z, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this CTA's shared
 // memory to a shared-memory address of a CTA of the cluster, counted on that CTA's mbarrier.
 __device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
@@ -259,14 +248,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-
-// Arrive on `bar` (same offset) in every CTA of cta_mask once this thread's tcgen05 work is done.
-__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
-        : "memory");
 }
 
 // Copy 32 rows x 128 bits from shared memory into TMEM, replicated into all four 32-lane

@@ -106,61 +106,6 @@ def test_grouped_every_plan(cfg, split, few_sms, monkeypatch):
     assert_within_tolerance(got[rows], want[rows], f"masked {cfg} split {split}")
 
 
-@pytest.mark.parametrize("cfg", CONFIGS)
-def test_dense_pair_multicast(cfg, few_sms, monkeypatch):
-    # CTA pairs on adjacent m-blocks share each B tile by TMA multicast (5 m-blocks: the last
-    # pair has one block past M).
-    monkeypatch.setenv("DG_FORCE_CONFIG", cfg)
-    monkeypatch.setenv("DG_FORCE_SPLIT", "1")
-    monkeypatch.setenv("DG_FORCE_PAIR", "1")
-    M, N, K = 600, 704, 1536
-    w, sfa, sfb, want = _dense(M, N, K, seed=len(cfg) + 77)
-    d = torch.full((M, N), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
-    _call_or_skip(dg.dg_fp8_gemm_nt, to_dev(w["a"]), to_dev(sfa), to_dev(w["b"]), to_dev(sfb), d)
-    dg.dg_check_device_error()
-    assert_within_tolerance(bits(d), want, f"{cfg} pair")
-
-
-@pytest.mark.parametrize("cfg", ["config_bn256_s4_a1", "config_bn128_s6_a2", "config_bn64_s8_a2"])
-def test_grouped_pair_multicast(cfg, few_sms, monkeypatch):
-    monkeypatch.setenv("DG_FORCE_CONFIG", cfg)
-    monkeypatch.setenv("DG_FORCE_SPLIT", "1")
-    monkeypatch.setenv("DG_FORCE_PAIR", "1")
-    # expert 0 has one block, expert 1 two: the first pair straddles experts (no multicast),
-    # then a padding-only block pair, then a pair with one block past M_sum
-    c = synth.make_contiguous(3, 256, 1024, tokens=0, seed=8, counts=[100, 200, 0])
-    extra = 128
-    c["m_indices"] = np.concatenate([c["m_indices"], np.full(extra, -1, np.int32)])
-    c["a"] = np.concatenate([c["a"], np.full((extra, c["K"]), 0x7F, np.uint8)])
-    c["sfa"] = np.concatenate([c["sfa"], np.ones((extra, c["K"] // 128), np.float32)])
-    c["M_sum"] += extra
-    csfa = oracle.pack_sf_ue8m0(c["sfa"], c["M_sum"], 1)[0]
-    csfb = oracle.pack_sf_ue8m0(c["sfb"], 256, 128)
-    d = torch.full((c["M_sum"], 256), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
-    _call_or_skip(dg.dg_m_grouped_fp8_gemm_nt_contiguous, to_dev(c["a"]), to_dev(csfa), to_dev(c["b"]),
-                  to_dev(csfb), d, to_dev(c["m_indices"]))
-    dg.dg_check_device_error()
-    got = bits(d)
-    valid = c["m_indices"] >= 0
-    assert np.all(got[~valid] == 0)
-    want = oracle.m_grouped_fp8_gemm_nt_contiguous(c["a"], csfa, c["b"], csfb, c["m_indices"])
-    assert_within_tolerance(got[valid], want[valid], f"contiguous pair {cfg}")
-
-    m = synth.make_masked(4, 384, 320, 1024, seed=9, masked_m=[384, 1, 0, 257])
-    msfa = oracle.pack_sf_ue8m0(m["sfa"], 384, 1)
-    msfb = oracle.pack_sf_ue8m0(m["sfb"], 320, 128)
-    md = torch.full((4, 384, 320), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
-    dg.dg_m_grouped_fp8_gemm_nt_masked(to_dev(m["a"]), to_dev(msfa), to_dev(m["b"]), to_dev(msfb), md,
-                                      to_dev(m["masked_m"]))
-    dg.dg_check_device_error()
-    prior = np.full((4, 384, 320), synth.SENTINEL_BF16, np.uint16)
-    want = oracle.m_grouped_fp8_gemm_nt_masked(m["a"], msfa, m["b"], msfb, m["masked_m"], prior)
-    got = bits(md)
-    rows = np.arange(384)[None, :] < m["masked_m"][:, None]
-    assert np.array_equal(got[~rows], want[~rows])
-    assert_within_tolerance(got[rows], want[rows], f"masked pair {cfg}")
-
-
 @pytest.mark.parametrize("cfg", ["config_bn224_s3_m2", "config_bn192_s3_m2", "config_bn208_s3_m2"])
 def test_contiguous_256_row_tiles_straddling_experts(cfg, few_sms, monkeypatch):
     # 256-row tiles (two 128-row halves): expert 0 has one block and expert 1 two, so the first
