@@ -3,8 +3,9 @@ configurations) the benchmark times, checked against the oracle.
 
 The decode shapes and the masked MoE workload are compared in full.  For the prefill GEMM
 (4096 x 7168 x 16384) and the contiguous MoE GEMM (33k rows x 4096 x 7168) the oracle computes
-a sample of rows (covering every 128-row block, with all columns); every element of the GPU
-result is additionally checked to be finite, and every padding row to be bit-exact +0.0.
+a sample of at least 512 full rows (covering every 128-row block, its first and last row, with
+all columns); every element of the GPU result is additionally checked to be finite, and every
+padding row to be bit-exact +0.0.
 """
 import numpy as np
 import pytest
@@ -25,7 +26,11 @@ def _gpu_packed(sf, mn, gran, groups=None):
     return out
 
 
+MIN_SAMPLED_ROWS = 512
+
+
 def _sample_rows(nrows, per_block, seed):
+    """The first and last row of every 128-row block plus `per_block` distinct random rows of it."""
     rs = np.random.default_rng(seed)
     rows = []
     for b0 in range(0, nrows, 128):
@@ -58,7 +63,8 @@ def test_prefill_sampled_rows():
     dg.dg_check_device_error()
     got = bits(d)
     assert np.all(np.isfinite(oracle.bf16_bits_to_float(got)))
-    rows = _sample_rows(M, 2, seed=1)
+    rows = _sample_rows(M, 16, seed=1)
+    assert rows.size >= MIN_SAMPLED_ROWS
     sfa_ref = oracle.pack_sf_ue8m0(w["sfa"][rows], rows.size, 1)[0]
     sfb_ref = oracle.pack_sf_ue8m0(w["sfb"], N, 128)[0]
     want = oracle.fp8_gemm_nt(w["a"][rows], sfa_ref, w["b"], sfb_ref)
@@ -78,8 +84,9 @@ def test_contiguous_moe_sampled_rows():
     m_idx = w["m_indices"]
     assert np.all(got[m_idx < 0] == 0), "padding rows must be +0.0"
     assert np.all(np.isfinite(oracle.bf16_bits_to_float(got[m_idx >= 0])))
-    rows = _sample_rows(M_sum, 1, seed=2)
+    rows = _sample_rows(M_sum, 2, seed=2)
     rows = rows[m_idx[rows] >= 0]
+    assert rows.size >= MIN_SAMPLED_ROWS
     sfa_ref = oracle.pack_sf_ue8m0(w["sfa"], M_sum, 1)[0]
     sfb_ref = oracle.pack_sf_ue8m0(w["sfb"], N, 128)
     want = oracle.m_grouped_fp8_gemm_nt_contiguous(w["a"], sfa_ref, w["b"], sfb_ref, m_idx, rows=rows)
@@ -153,7 +160,8 @@ def test_nn_layout_fp32_accumulate_prefill_sampled_rows():
     dg.dg_check_device_error()
     got = d.cpu().numpy()
     assert np.all(np.isfinite(got))
-    rows = _sample_rows(M, 2, seed=11)
+    rows = _sample_rows(M, 16, seed=11)
+    assert rows.size >= MIN_SAMPLED_ROWS
     want = oracle.fp8_gemm(w["a"][rows], oracle.pack_sf_ue8m0(w["sfa"][rows], len(rows), 1)[0], b_nn, sfb,
                            layout="nn", c=c[rows], out="f32")
     from tests._parity import assert_close_f32
