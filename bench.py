@@ -1,14 +1,19 @@
 """Benchmark of the FP8 block-scaled GEMM hot path on GB300 (one JSON line on stdout).
 
 A step is one pass of the whole hot path over one batch of synthetic inputs: for each
-workload of the suite, the scale factors of both operands are packed on the GPU
+workload of the suite, the activations' scale factors are packed on the GPU
 (dg_pack_sf_ue8m0) and the GEMM runs (dense, contiguous-grouped or masked-grouped).  The
-suite (shapes from the DeepGEMM article's H800 tables):
+weights' scale factors are packed once, when the weights are set up (the packed layout is a
+one-time transform of a static tensor), and stay resident like the weights.  The suite
+(shapes from the DeepGEMM article's H800 tables):
     decode 64x2112x7168, 128x24576x1536, 128x7168x2048, 64x4096x7168  (dense, A with 1 % x20 outliers)
     prefill 4096x7168x16384                                            (dense)
     contiguous MoE: 4 experts, N=4096, K=7168, 32768 tokens (multinomial), segments padded to 128
     masked MoE: 4 groups, max_m=256, N=7168, K=2048, masked_m ~ U{1..256}
 value = total valid FLOPs of all GEMMs / device time, in TFLOPS.
+
+The small dense GEMM 128x512x1024 is timed beside the step as its own latency-bound row
+(`workloads`, marked "in_value": false): it is not part of `value`.
 
 L2: every GEMM's operands were last touched one step earlier, and one step streams about
 1 GB, far more than the 129 MB L2, so every timed GEMM reads cold operands.
@@ -46,6 +51,7 @@ WORKLOAD_NAME = ("fp8 block-scaled GEMM suite: decode 64x2112x7168, 128x24576x15
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor ratio (4.5 / 2.25 PFLOP/s)
+MMA_MACS_PER_CLK_SM = 8192   # FP8 block-scaled MMA rate of one SM, measured on GB300
 
 
 # ---------------------------------------------------------------------------
@@ -75,6 +81,16 @@ def make_workloads(seed: int = 0):
         w["flops"] = 2.0 * w["valid_rows"] * w["N"] * w["K"]
         w["bytes"] = _algorithmic_bytes(w)
     return ws
+
+
+def suite_config(ws, world: int) -> dict:
+    """The `config` object of the JSON line; both arms print the same one."""
+    return {"workload": WORKLOAD_NAME, "flops_per_step": sum(w["flops"] for w in ws),
+            "bytes_per_step": sum(w["bytes"] for w in ws),
+            "weights": "packed weight scales resident (packed once at set-up); activation scales packed every step",
+            "l2": "cold operands: each GEMM's inputs were last touched one step earlier and a step "
+                  "streams ~1 GB (> 129 MB L2)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def _valid_rows(w) -> int:
@@ -135,10 +151,14 @@ class DeviceWorkload:
             self.idx = t(w["masked_m"])
         self.N = N
 
+    def pack_weights(self):
+        """The weights' scales, packed once at set-up (outside every timed region)."""
+        self.dg.dg_pack_sf_ue8m0(self.sfb_f, self.sfb, self.N, 128)
+
     def pack(self, io=None):
+        """The activations' scales, packed every step."""
         sfa_f = self.sfa_f if io is None else io["sfa_f"]
         self.dg.dg_pack_sf_ue8m0(sfa_f, self.sfa, self.rows_a, 1)
-        self.dg.dg_pack_sf_ue8m0(self.sfb_f, self.sfb, self.N, 128)
 
     def gemm(self, io=None):
         dg = self.dg
@@ -310,6 +330,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     torch.cuda.set_device(dev)
     ws = make_workloads(seed=0)
     dws = [DeviceWorkload(w, dev) for w in ws]
+    for dw in dws:
+        dw.pack_weights()
     stream = torch.cuda.current_stream()
 
     def step(events=None, only=None):
@@ -397,6 +419,13 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     roof["kernel"] = dw_["name"]
     roof["peak_source"] = peak_label if roof["bound"] == "tensor" else f"hbm copy (of {peaks['source']})"
     roof["algorithmic_per_launch"] = dw_["flops"] if roof["bound"] == "tensor" else dw_["bytes"]
+    if roof["bound"] == "tensor" and clocks.get("sm_mhz"):
+        # the tensor pipe's own rate at the clock seen during the timed region: 8192 FP8
+        # multiply-adds per cycle per SM (measured with back-to-back 128 x 256 x 32 MMAs)
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        clock_peak = 2.0 * MMA_MACS_PER_CLK_SM * n_sm * clocks["sm_mhz"] * 1e6 / 1e12
+        roof["clock_mma_peak"] = round(clock_peak, 1)
+        roof["frac_of_clock_mma"] = round(roof["achieved"] / clock_peak, 4)
 
     # end to end, through the same public calls, inputs from pinned host memory
     e2e = None
@@ -437,6 +466,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                       "step's GEMMs; weights resident"}
 
     time_hbm_streams(ws, dws, per_wl, peaks)
+    for pw in per_wl:
+        pw["in_value"] = True
+    per_wl.append(time_small_dense(dev, peaks))
     next_rows = None if args.no_next else time_next_rows(dev, peaks)
 
     cpu = None
@@ -445,16 +477,12 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
 
     if rank != 0:
         return None
-    launches_per_step = 3 * len(dws)
+    launches_per_step = 2 * len(dws)        # activation-scale pack + GEMM per workload
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAME, "flops_per_step": flops_step,
-                   "bytes_per_step": sum(w["bytes"] for w in ws),
-                   "l2": "cold operands: each GEMM's inputs were last touched one step earlier and a step "
-                         "streams ~1 GB (> 129 MB L2)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": suite_config(ws, world),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks, "workloads": per_wl, "next_rows": next_rows,
     }
@@ -553,6 +581,51 @@ def time_hbm_streams(ws, dws, per_wl, peaks):
                    "stream_frac": round(gbs / peaks["hbm_gbs"], 4), "stream_weight_copies": copies})
         del bs, sfbs
     dg.dg_check_device_error()
+
+
+def time_small_dense(dev, peaks, reps: int = 20):
+    """The small dense GEMM 128x512x1024 (A, B ~ N(0, 1), seed 0), timed beside the step as a
+    latency-bound row of its own: bracketed alone with L2 flushed before each rep, and back to
+    back inside one CUDA graph (16 launches per replay over 16 weight copies; they fit in L2).
+    Both fractions are reported, of the FP8 tensor peak and of HBM bandwidth."""
+    import moe_grouped_gemm_02_gb300 as dg
+    M, N, K = synth.SMALL_DENSE
+    w = synth.make_dense(M, N, K, seed=0)
+    w["kind"] = "dense"
+    w["valid_rows"] = M
+    dw = DeviceWorkload(w, dev)
+    dw.pack_weights()
+    dw.pack()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        dw.gemm()
+    ms, lo, hi = _time_launches(dw.gemm, stream, flush, reps)
+    copies = 16
+    bs = [dw.b.clone() for _ in range(copies)]
+    sfbs = [dw.sfb.clone() for _ in range(copies)]
+    sms = _graph_stream_ms(lambda i, st: dg.dg_fp8_gemm_nt(dw.a, dw.sfa, bs[i], sfbs[i], dw.d, stream=st), copies)
+    dg.dg_check_device_error()
+    flops = 2.0 * M * N * K
+    nbytes = _algorithmic_bytes(w)
+    fp8_peak = peaks["bf16"] * FP8_OVER_BF16
+
+    def rates(t_ms):
+        tf = flops / (t_ms * 1e-3) / 1e12
+        gbs = nbytes / (t_ms * 1e-3) / 1e9
+        return tf, gbs
+
+    tf, gbs = rates(ms)
+    stf, sgbs = rates(sms)
+    del flush, bs, sfbs
+    return {"workload": f"small_dense_{M}x{N}x{K}", "in_value": False, "bound": "latency",
+            "ms": round(ms, 5), "ms_min": round(lo, 5), "ms_max": round(hi, 5), "us": round(ms * 1e3, 2),
+            "flops": flops, "bytes": nbytes, "tflops": round(tf, 2), "gbs": round(gbs, 1),
+            "frac_tensor": round(tf / fp8_peak, 4), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "stream_ms": round(sms, 5), "stream_tflops": round(stf, 2), "stream_gbs": round(sgbs, 1),
+            "stream_frac_tensor": round(stf / fp8_peak, 4), "stream_frac_hbm": round(sgbs / peaks["hbm_gbs"], 4),
+            "how": "bracketed: alone, L2 flushed before each of 20 reps (median); stream: back to back in one "
+                   "CUDA graph over 16 weight copies (L2-resident)"}
 
 
 def _random_e4m3(shape, gen, dev):
@@ -759,7 +832,7 @@ def run_reference(args, rank: int, world: int):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed * 1e3 / max(1, args.steps), 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_NAME, "sample": "1 output row per workload per step"},
+            "config": suite_config(ws, world),
             "cpu_baseline": cpu, "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                                          "d2h_bytes_per_step": 0}}
 
