@@ -51,7 +51,8 @@ const KernelConfig* const* all_configs(int* n) {
     static const KernelConfig* cfgs[] = {&config_bn256_s4_a1(), &config_bn224_s4_a2(),
                                          &config_bn192_s5_a2(), &config_bn128_s6_a2(), &config_bn128_s4_a2(), &config_bn64_s8_a2(),
                                          &config_bn32_s8_a2(), &config_bn224_s3_m2(), &config_bn192_s3_m2(),
-                                         &config_bn208_s3_m2(), &config_bn128_s5_k2(), &config_bn192_s5_k2()};
+                                         &config_bn208_s3_m2(), &config_bn128_s5_k2(), &config_bn192_s5_k2(),
+                                         &config_bn128_s8_k2_r64()};
     *n = static_cast<int>(sizeof(cfgs) / sizeof(cfgs[0]));
     return cfgs;
 }
@@ -182,7 +183,7 @@ int cluster_capacity(DeviceState& st, int cfg_index, const KernelConfig* c, int 
 }
 
 Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N, int kblocks, int sms,
-                 int extra_ints, int b_mn, int b_fp4) {
+                 int extra_ints, int a_mn, int b_mn, int b_fp4) {
     int n = 0;
     const KernelConfig* const* cfgs = all_configs(&n);
     // DG_FORCE_CONFIG=<name>, DG_FORCE_SPLIT=<1|2|4|8> pin the plan (tuning).
@@ -196,6 +197,9 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
         if (force_cfg && std::strcmp(force_cfg, c->name) != 0) continue;
         for (int split : {1, 2, 4, 8}) {
             if (fsplit && split != fsplit) continue;
+            // 64-row A stages serve calls with at most 64 rows of K-major A (dense M, masked max_m)
+            if (c->a_rows < 128 && (rows > c->a_rows || a_mn || (mode != MODE_DENSE && mode != MODE_MASKED)))
+                continue;
             // MN-major B is loaded in boxes of 128 columns; K-grouped tiles have per-group K.
             if (b_mn && c->bn % 128 != 0 && c->mh != 2) continue;
             if (mode == MODE_K_GROUPED && split > 1) continue;
@@ -221,7 +225,7 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
             const double kb_per = static_cast<double>((kblocks + split - 1) / split);
             // an MN-major B arrives in whole 128-column boxes
             const double b_rows = b_mn ? 128.0 * ((c->bn + 127) / 128) : c->bn;
-            const double tma = 2.2 * (128.0 * c->mh + b_rows);
+            const double tma = 2.2 * (static_cast<double>(c->a_rows) * c->mh + b_rows);
             // one issuer: max(161, N/2 + 33) per MMA; two issuers (MH = 2) keep the pipe at N/2 + 33;
             // K-split issuers (KS = 2) issue two MMAs each per stage, side by side
             const double mma = c->mh == 2   ? 8.0 * (c->bn / 2.0 + 33.0)
@@ -343,7 +347,7 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     const int plan_kb = kgrouped ? std::max(1, (Kb + groups - 1) / groups) : Kb;
     const int kp_rows = kgrouped ? Kb / 4 + groups : Kp;
     const Plan plan =
-        choose_plan(*st, mode, rows, m_blocks * groups, N, plan_kb, sms, extra_ints, call.b_mn, call.b_fp4);
+        choose_plan(*st, mode, rows, m_blocks * groups, N, plan_kb, sms, extra_ints, call.a_mn, call.b_mn, call.b_fp4);
     if (!plan.cfg) return DG_ERR_SHAPE;   // nothing fits in shared memory (too many groups)
     const KernelConfig* cfg = plan.cfg;
 
@@ -357,7 +361,7 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     bool ok = call.a_mn ? encode_3d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, rows, Km, a_groups, 128, 128,
                                     CU_TENSOR_MAP_SWIZZLE_128B)
                         : encode_3d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a, Km, rows, a_groups, 128,
-                                    128 * cfg->mh, CU_TENSOR_MAP_SWIZZLE_128B);
+                                    cfg->a_rows * cfg->mh, CU_TENSOR_MAP_SWIZZLE_128B);
     if (call.b_fp4) {
         // E2M1 B, K-major: the TMA unpacks each 8 bytes (16 values) into a 16-byte unit, so a
         // 128-value box row fills a 128-byte swizzled row as an E4M3 row does.
@@ -414,6 +418,18 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     args.debug_drop_stage = -1;
     args.pdl = pdl_enabled();
     args.tma_store = plan.tma_store;
+    // Weights well inside L2 (decode and masked shapes): each CTA warms L2 with its first
+    // tile's B slice before waiting for the previous kernel (DG_PREFETCH_B=0 disables it).
+    {
+        const double b_bytes = static_cast<double>(b_groups) * N * static_cast<double>(K) * (call.b_fp4 ? 0.5 : 1.0);
+        const char* pf = std::getenv("DG_PREFETCH_B");
+        const bool pf_on = !(pf && pf[0] == '0');
+        args.prefetch_b = (pf_on && !call.b_mn && (mode == MODE_DENSE || mode == MODE_MASKED) &&
+                           b_bytes <= 64.0 * 1024 * 1024) ? 1 : 0;
+    }
+    // D += A @ B^T in place: the epilogue's FP32 boxes are added to D by TMA reductions
+    args.c_reduce = (call.out_f32 && call.c != nullptr && static_cast<const void*>(call.c) == call.d &&
+                     plan.tma_store) ? 1 : 0;
     if (const char* t = std::getenv("DG_DEBUG_DROP_LOAD")) args.debug_drop_stage = std::atoi(t);
     args.num_m_units = cfg->mh == 2 ? (m_blocks + 1) / 2 : m_blocks;
     long long units_upper = static_cast<long long>(args.num_m_units) * groups * args.num_n_blocks;

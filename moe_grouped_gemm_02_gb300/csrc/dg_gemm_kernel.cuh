@@ -57,13 +57,19 @@ constexpr uint32_t SF_WARP = 6;      // warp that re-lays scale words for tcgen0
 constexpr uint32_t MMA1_WARP = 7;    // second MMA issuer (MH = 2 or KS = 2)
 constexpr int DG_ERR_TIMEOUT_CODE = 6;
 
-template <int BN_, int STAGES_, int ACC_, int MH_ = 1, int KS_ = 1>
+template <int BN_, int STAGES_, int ACC_, int MH_ = 1, int KS_ = 1, int AR_ = 128>
 struct GemmCfg {
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
     static constexpr int ACC = ACC_;
     static constexpr int MH = MH_;                      // 128-row halves of a tile
     static constexpr int TM = BM * MH;                  // rows of a tile
+    // A rows loaded per stage and 128-row half: 128, or 64 for calls with at most 64 rows of A
+    // (the M = 64 decode shapes), which leaves room for a deeper ring of B tiles.  The MMA still
+    // reads 128 rows; rows 64-127 then come from the next buffer in shared memory and give
+    // accumulator rows that are never stored or exchanged.
+    static constexpr int AR = AR_;
+    static_assert(AR == 128 || (AR == 64 && MH_ == 1), "64-row A stages only with one 128-row half");
     // KS = 2: two MMA issuers split each 128-K stage (K steps 0-1 and 2-3) into the two TMEM
     // accumulators, which the epilogue adds.  One thread issues at most one block-scaled MMA
     // per ~161 cycles whatever its N, so for the narrow tiles of the HBM-bound shapes (N = 128,
@@ -85,7 +91,7 @@ struct GemmCfg {
     // Accumulators start on 32-column boundaries: BN columns each, ACC_STRIDE apart.
     static constexpr int ACC_STRIDE = (BN + 31) / 32 * 32;
     static constexpr int SFB_CHUNKS = (BN + 127) / 128;   // 128-row scale chunks of a B tile
-    static constexpr int A_BYTES = TM * BK;
+    static constexpr int A_BYTES = MH * AR * BK;
     static constexpr int B_BYTES = BN * BK;
     // An MN-major B tile arrives in boxes of 128 columns (the 128-byte swizzle span): with
     // MH = 2 the stage holds whole boxes, so that BN = 224 or 192 take an MN-major B too (the
@@ -119,14 +125,14 @@ struct GemmCfg {
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
     static constexpr int OFF_CUM = OFF_MISC + 16;             // masked mode: m-unit prefix sums
     // Split-K receive buffer: one slot per other CTA of the cluster, each holding the (at most
-    // 128 / split) rows this CTA owns, BN FP32 per row (rows padded by 16 bytes).
+    // AR / split) rows this CTA owns, BN FP32 per row (rows padded by 16 bytes).
     static constexpr int RECV_ROW = BN * 4 + 16;
     static __host__ __device__ uint32_t off_recv(int extra_ints) {
         return (static_cast<uint32_t>(OFF_CUM + extra_ints * 4) + 15u) & ~15u;
     }
     static_assert(128 * RECV_ROW <= OFF_SFA, "split-K staging of a whole tile fits in the operand ring");
     static __host__ __device__ uint32_t recv_bytes(int split) {
-        return split > 1 ? static_cast<uint32_t>((split - 1) * (BM / split) * RECV_ROW) : 0u;
+        return split > 1 ? static_cast<uint32_t>((split - 1) * (AR / split) * RECV_ROW) : 0u;
     }
     // Without split-K the space after the prefix sums stages the epilogue's output boxes: two
     // 1 KB buffers per epilogue warp (32 rows x 32 bytes each), the source of TMA bulk stores,
@@ -499,11 +505,47 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tmem_alloc(base + C::OFF_MISC, C::TMEM_COLS);
         tmem_relinquish();
     }
-    // Everything above touches only this CTA's shared and tensor memory, so with programmatic
-    // dependent launch it overlaps the previous kernel; no global memory is read before this.
-    griddep_wait();
+    if (args.prefetch_b && warp == 0 && lane == 0) {
+        // Warm L2 with the B tiles and the scale words of this CTA's first unit (its K range of
+        // one tile) while the previous kernel finishes: a prefetch reads nothing into this CTA,
+        // so it is safe before the dependency wait even if that kernel writes these tensors.
+        // Dense calls know their first unit here; masked calls do not (the unit map needs
+        // masked_m), so they assume one m-unit per group, which names the first units' tiles
+        // when groups are shallow and only warms other ones otherwise.
+        const int crank0 = split > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+        const int u0 = split > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+        int nb = -1, mb = 0, g = 0;
+        if (args.mode == MODE_DENSE) {
+            if (u0 < args.num_units) {
+                const int per_band = args.num_m_units * args.raster_n;
+                const int band = u0 / per_band;
+                const int r = u0 - band * per_band;
+                const int n0 = band * args.raster_n;
+                const int width = min(args.raster_n, args.num_n_blocks - n0);
+                mb = r / width;
+                nb = n0 + (r - mb * width);
+            }
+        } else if (args.mode == MODE_MASKED && u0 < args.groups * args.num_n_blocks) {
+            g = u0 / args.num_n_blocks;
+            nb = u0 - g * args.num_n_blocks;
+        }
+        if (nb >= 0) {
+            const int k0 = crank0 * args.kblocks / split, k1 = (crank0 + 1) * args.kblocks / split;
+            for (int kp = k0 >> 2; kp <= (k1 - 1) >> 2 && k1 > k0; ++kp) {
+                tma_prefetch_l2_3d(&tm_sfb, nb * C::BN, kp, g);
+                tma_prefetch_l2_3d(&tm_sfa, mb * C::TM, kp, g);
+            }
+            for (int kb = k0; kb < k1; ++kb) tma_prefetch_l2_3d(&tm_b, kb * BK, nb * C::BN, g);
+        }
+    }
+    // Programmatic dependent launch: the next kernel in the stream may start launching now (its
+    // CTAs still wait for this grid to complete before they touch its outputs).  Everything up
+    // to each role's griddep_wait() touches only this CTA's shared and tensor memory (and L2,
+    // by the prefetch), so it overlaps the previous kernel: every thread that reads or writes
+    // global memory waits for that kernel first, right before its first such access.
     griddep_launch_dependents();
     if (args.mode == MODE_MASKED && warp == 2) {
+        griddep_wait();
         // cum[g] = sum over g' < g of the m-units of group g' (128*MH-row tiles): each lane sums a contiguous run of groups, then an exclusive warp
         // scan over the runs.
         const int G = args.groups;
@@ -529,6 +571,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (lane == 31) cum[G] = incl;
     }
     if (args.mode == MODE_K_GROUPED && warp == 2) {
+        griddep_wait();
         // cum[g] = sum over g' < g of ks[g'] / 128 (K blocks) and cum[G + 1 + g] the same sum of
         // ceil(ks[g'] / 512) (packed scale-word rows): two exclusive warp scans over runs.
         const int G = args.groups;
@@ -603,6 +646,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             uint32_t ph = 0;
             uint32_t issued = 0;   // stages issued in total (for the abort drain)
             bool ok = true;
+            // (contiguous units read m_indices; other modes wait right before the first load,
+            // after the first stage's barrier is armed)
+            bool waited = args.mode == MODE_CONTIGUOUS;
+            if (waited) griddep_wait();
             for (int u = u_first; ok && u < total_units; u += u_step) {
                 const Unit t = decode_unit<MH>(args, cum, u, kb0, kb1);
                 if (t.zero) continue;
@@ -627,6 +674,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                                           : C::TX_AB);
                     const int kx = (t.koff + kb) * BK;
                     const int gbz = args.mode == MODE_K_GROUPED ? 0 : t.gb;
+                    if (!waited) {
+                        griddep_wait();
+                        waited = true;
+                    }
                     if (!args.a_mn) {
                         tma_load_3d(base + C::OFF_A + s * C::A_BYTES, &tm_a, fb, kx, t.mb * C::TM, ga);
                     } else {
@@ -669,6 +720,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // steps 2h and 2h + 1 of every stage into accumulator h (KS = 2); a unit whose half h is
         // inactive still walks every barrier (issuing no MMA) to stay in step.
         if (lane == 0) {
+            if (args.mode == MODE_CONTIGUOUS) griddep_wait();   // units read m_indices
             const uint32_t h = warp == 1 ? 0u : 1u;
             int s = 0;
             uint32_t ph = 0;
@@ -776,6 +828,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         int sf_slot = 0;
         uint32_t sff_phbits = 0;
         uint32_t sfe_phbits = 0;          // bit j: parity of scale slot j's empty barrier
+        bool waited = args.mode == MODE_CONTIGUOUS;   // units read m_indices
+        if (waited) griddep_wait();
         int sf_last = -1;                 // last scale slot loaded (for the abort drain)
         uint32_t sf_last_par = 0;
         bool ok = true;
@@ -790,6 +844,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         const uint32_t sb = sffull_bar(sf_slot);
                         mbar_arrive_expect_tx(sb, C::TX_SF);
                         const int kp = t.kpoff + grp;
+                        if (!waited) {
+                            griddep_wait();
+                            waited = true;
+                        }
                         tma_load_3d(base + C::OFF_SFA + sf_slot * C::SFA_BYTES, &tm_sfa, sb, t.mb * C::TM, kp, ga);
                         tma_load_3d(base + C::OFF_SFB + sf_slot * C::SFB_BYTES, &tm_sfb, sb, t.nb * C::BN, kp,
                                     args.mode == MODE_K_GROUPED ? 0 : t.gb);
@@ -829,12 +887,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // ------------------------------------------------------------------ epilogue
         // Warps 2-5 write half 0 of each tile, warps 8-11 half 1 (MH = 2) or the second half of
         // the columns (EPI_COLS = 2).
+        griddep_wait();
         const uint32_t q = warp & 3u;                 // the TMEM lane quadrant this warp may read
         const int my_half = (MH == 2 && warp >= 8) ? 1 : 0;
         constexpr int NCH = (C::BN + 31) / 32;        // 32-column chunks of a tile row
         const int my_cols = (C::EPI_COLS == 2 && warp >= 8) ? 1 : 0;
         const int ch_lo = my_cols * NCH / C::EPI_COLS, ch_hi = (my_cols + 1) * NCH / C::EPI_COLS;
         const bool use_c = args.out_f32 && args.c != nullptr;
+        // In place (C is D): the FP32 boxes are reduce-added into D by the TMA, so C is never
+        // loaded on the box path, and a tile with nothing computed leaves D as it is.
+        const bool c_red = use_c && args.c_reduce != 0;
         // This warp's two 1 KB output staging buffers (no split-K: the receive region is free).
         const uint32_t ew = warp <= 5 ? warp - 2u : warp - 4u;     // epilogue warp index 0..7
         const uint32_t stage_out = base + C::off_stage_out(extra_smem_ints(args.mode, args.groups)) + ew * 2048u;
@@ -846,6 +908,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         uint32_t red_eph = 0;  // split-K: parity of the slot-free barriers
         uint32_t red_dph = 0;  // split-K: parity of the unit-done barrier
         uint32_t red_fmask = 0;  // split-K: parities of the four receive barriers
+        // split-K: this warp has arrived on the final cluster barrier (on its last unit, once the
+        // peers' partial rows have landed here, so that the barrier's latency overlaps the sums
+        // and stores; it only waits at exit)
+        bool final_arrived = false;
         for (int u = u_first; u < total_units; u += u_step) {
             if (misc[1]) break;
             const Unit t = decode_unit<MH>(args, cum, u, kb0, kb1);
@@ -888,10 +954,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 bool write, zero_row;
                 row_state(row, write, zero_row);
                 const size_t row_off = roff_of(row);
-                const uint32_t V = static_cast<uint32_t>(min(BM, max(0, m_valid - t.mb * BM)));
+                const uint32_t V = static_cast<uint32_t>(min(C::AR, max(0, m_valid - t.mb * BM)));
                 const uint32_t usplit = static_cast<uint32_t>(split);
                 const uint32_t RPO = V > 0 ? (V + usplit - 1) / usplit : 1u;
-                const uint32_t RPO_CAP = BM / usplit;                // rows of a receive slot
+                const uint32_t RPO_CAP = C::AR / usplit;             // rows of a receive slot
                 const uint32_t r_in_tile = q * 32u + lane;
                 const bool valid_row = r_in_tile < V;
                 const uint32_t owner = valid_row ? r_in_tile / RPO : crank;
@@ -980,6 +1046,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                                        misc + 1, args.err, args.timeout_ns, SITE_RED_FULL);
                     if (!landed) break;
                     for (uint32_t qq = qr0; qq < qr1; ++qq) red_fmask ^= 1u << qq;
+                    // Everything the peers send here has landed, and the peers arrive only once
+                    // this CTA's rows have landed there: the final barrier may count this warp.
+                    __syncwarp();
+                    cluster_arrive();
+                    final_arrived = true;
                     constexpr uint32_t UPR = C::BN / 8;               // 16-byte units per row
                     const uint32_t et = (warp - 2u) * 32u + lane;     // epilogue thread 0..127
                     for (uint32_t i = et; i < (own1 - own0) * UPR; i += static_cast<uint32_t>(C::EPI_THREADS)) {
@@ -1090,7 +1161,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             if (t.zero) {
                 // Padding only: zeros for every row of the tile, no accumulator involved.
-                {
+                if (!c_red) {
                     const int h = my_half;
                     const int row = row_of(h);
                     bool write, zero_row;
@@ -1100,7 +1171,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 continue;
             }
             float4 cv_next[8];    // FP32 with C: the next chunk's C values
-            if (use_c && ((t.hmask >> my_half) & 1u)) {
+            if (use_c && !c_red && ((t.hmask >> my_half) & 1u)) {
                 // Ask L2 for this thread's C segment, and load its first chunk, while the tile's
                 // main loop still runs.
                 const int row = row_of(my_half);
@@ -1140,7 +1211,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_3d(&tm_d, buf, col, slab0, t.g);
+                        if (c_red) tma_reduce_add_3d(&tm_d, buf, col, slab0, t.g);
+                        else tma_store_3d(&tm_d, buf, col, slab0, t.g);
                         bulk_commit_group();
                     }
                     ++nbox;
@@ -1157,8 +1229,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     uint32_t pk[NP * 8];
                     // 32 columns per TMEM load (half the round trips) where registers allow: with
                     // 384 threads a thread has at most 168, and K-split kernels load two
-                    // accumulators, so those load 16 at a time.
-                    constexpr int LDC = (C::THREADS <= 256 && C::KS == 1) ? 32 : 16;
+                    // accumulators, so those with more than 128 columns load 16 at a time.
+                    constexpr int LDC = (C::THREADS <= 256 && (C::KS == 1 || C::BN <= 128)) ? 32 : 16;
                     auto load_pieces = [&](int i, auto width) {   // pieces i (and i + 1 when 32 wide)
                         uint32_t r[32];
                         const uint32_t col = t_row + 16u * static_cast<uint32_t>(pc0 + i);
@@ -1244,10 +1316,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     float4 cv[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) cv[j] = cv_next[j];
-                    if (use_c && write && c + 1 < ch_hi) load_c_chunk(args, row_off, n0 + 32 * (c + 1), N, 32, cv_next);
+                    if (use_c && !c_red && write && c + 1 < ch_hi)
+                        load_c_chunk(args, row_off, n0 + 32 * (c + 1), N, 32, cv_next);
                     tmem_wait_ld();
                     if (!slab_tma) {
-                        if (write) store_row_chunk(args, row_off, n0 + 32 * c, N, r, ncols, zero_row, use_c ? cv : nullptr);
+                        // (in place, C is loaded here: it was not loaded ahead)
+                        if (write)
+                            store_row_chunk(args, row_off, n0 + 32 * c, N, r, ncols, zero_row,
+                                            (use_c && !c_red) ? cv : nullptr);
                         continue;
                     }
                     // One box = 32 rows x 32 bytes: 16 BF16 or 8 FP32 columns (fully unrolled so
@@ -1264,7 +1340,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                 v1 = make_float4(__uint_as_float(r[8 * b + 4]), __uint_as_float(r[8 * b + 5]),
                                                  __uint_as_float(r[8 * b + 6]), __uint_as_float(r[8 * b + 7]));
                             }
-                            if (use_c && write) {
+                            if (use_c && !c_red && write) {
                                 v0.x += cv[2 * b].x, v0.y += cv[2 * b].y, v0.z += cv[2 * b].z, v0.w += cv[2 * b].w;
                                 v1.x += cv[2 * b + 1].x, v1.y += cv[2 * b + 1].y, v1.z += cv[2 * b + 1].z,
                                     v1.w += cv[2 * b + 1].w;
@@ -1302,6 +1378,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (lane == 0 && nbox > 0) bulk_wait_group_all();   // D is written before the CTA ends
         __syncwarp();
+        if (final_arrived) {
+            // the final barrier: this warp arrived early; wait with everyone else
+            tc_fence_before_sync();
+            if (clustered) cluster_wait();
+            return;   // (TMEM is freed by warp 1 after the same barrier)
+        }
     }
 
     tc_fence_before_sync();
@@ -1395,13 +1477,14 @@ cudaError_t prepare_fp8_gemm(int max_smem) {
     return prep(fp8_gemm_kernel<C, V ? SPEC_MASKED_FP4 : SPEC_ANY>);
 }
 
-#define DG_DEFINE_CONFIG_KS(FN, BN_, ST_, AC_, MH_, KS_)                                             \
-    const KernelConfig& FN() {                                                                        \
-        using C = GemmCfg<BN_, ST_, AC_, MH_, KS_>;                                                   \
-        static const KernelConfig cfg{BN_, ST_, AC_, MH_, KS_, #FN, &C::smem_bytes, &launch_fp8_gemm<C>, \
-                                      &prepare_fp8_gemm<C>, &max_clusters_fp8_gemm<C>};               \
-        return cfg;                                                                                   \
+#define DG_DEFINE_CONFIG_AR(FN, BN_, ST_, AC_, MH_, KS_, AR_)                                             \
+    const KernelConfig& FN() {                                                                             \
+        using C = GemmCfg<BN_, ST_, AC_, MH_, KS_, AR_>;                                                   \
+        static const KernelConfig cfg{BN_, ST_, AC_, MH_, KS_, AR_, #FN, &C::smem_bytes, &launch_fp8_gemm<C>, \
+                                      &prepare_fp8_gemm<C>, &max_clusters_fp8_gemm<C>};                    \
+        return cfg;                                                                                        \
     }
+#define DG_DEFINE_CONFIG_KS(FN, BN_, ST_, AC_, MH_, KS_) DG_DEFINE_CONFIG_AR(FN, BN_, ST_, AC_, MH_, KS_, 128)
 #define DG_DEFINE_CONFIG(FN, BN_, ST_, AC_, MH_) DG_DEFINE_CONFIG_KS(FN, BN_, ST_, AC_, MH_, 1)
 
 }  // namespace dg

@@ -42,6 +42,10 @@ struct GemmArgs {
     int debug_drop_stage;   // test hook: the producer skips this stage's loads (-1: never)
     int pdl;                // launch with programmatic dependent launch
     int tma_store;          // the epilogue writes D through its tensor map (else plain stores)
+    int prefetch_b;         // before its dependency wait, each CTA prefetches its first tile's B slice
+                            // into L2 (weights that fit in L2 many times over)
+    int c_reduce;           // FP32 C is D itself and D goes out through its tensor map: the epilogue's
+                            // boxes are added to D in place by TMA reductions (no C loads)
 };
 
 // Shared-memory ints after the barriers: the masked-mode m-unit prefix sums (G + 1) or the
@@ -60,6 +64,7 @@ struct KernelConfig {
     int acc;            // TMEM accumulator buffers
     int mh;             // 128-row halves per tile (2: one B tile serves 256 rows)
     int ks;             // MMA issuers splitting each stage's K steps (2: both accumulators serve one tile)
+    int a_rows;         // A rows loaded per 128-row half: 128, or 64 (calls with at most 64 rows of A)
     const char* name;
     size_t (*smem_bytes)(int extra_ints, int split, int tma_store);
     GemmLaunchFn launch;
@@ -80,6 +85,7 @@ const KernelConfig& config_bn192_s3_m2();
 const KernelConfig& config_bn208_s3_m2();
 const KernelConfig& config_bn128_s5_k2();
 const KernelConfig& config_bn192_s5_k2();
+const KernelConfig& config_bn128_s8_k2_r64();
 
 cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb, int Kb, int Kp,
                            int mn_al, int gran_mn, int pdl, cudaStream_t stream);

@@ -37,8 +37,38 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 
+// Elementwise unsigned maximum of two pairs of 16-bit halves.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Elementwise BF16 product of two pairs, rounded to nearest even.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Byte permute: the bytes of {b, a} picked by `sel` (four 4-bit indices).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
 constexpr int QUANT_WARPS = 8;
 
+// The arithmetic works on BF16 pairs as they are loaded:
+//  * the block amax is an unsigned maximum of the magnitude bits (sign cleared), two halves
+//    at a time, and both of a lane's blocks travel through one 16-lane butterfly (block i in
+//    half i);
+//  * the scaling by 2^-e is one BF16 pair product.  2^-e is a BF16 normal for every e a
+//    finite BF16 block can have (e in [-127, 120]) and BF16 has FP32's exponent range, so the
+//    product is exact whenever it is a normal number; a product below the normal range is
+//    under 2^-126 and rounds to a signed zero in E4M3 whichever way it was rounded before;
+//  * the two products are widened to FP32 (exactly) for the E4M3 conversion.
 __global__ void __launch_bounds__(32 * QUANT_WARPS)
     quantize_fp8_1x128_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ q, int32_t* __restrict__ sf,
                               int M, int K, int Kb, int Kp, int m_al, int row_groups) {
@@ -56,8 +86,8 @@ __global__ void __launch_bounds__(32 * QUANT_WARPS)
 
     const size_t row = static_cast<size_t>(g) * M + r;
     uint4 v[2];
-    uint32_t amax[2];
     bool valid[2];
+    uint32_t mx[2];   // per block: the two 16-bit halves' maximum magnitudes
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int kb = 4 * kp + 2 * i + (lane >> 4);
@@ -65,35 +95,33 @@ __global__ void __launch_bounds__(32 * QUANT_WARPS)
         v[i] = valid[i] ? __ldcs(reinterpret_cast<const uint4*>(x + row * K + 512 * kp + 256 * i + 8 * lane))
                         : make_uint4(0u, 0u, 0u, 0u);
         // |x| as BF16 magnitude bits; for finite values their integer order is the value order
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        uint32_t m = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) m = max(m, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
-#pragma unroll
-        for (int off = 1; off < 16; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-        amax[i] = m;
+        mx[i] = max_u16x2(max_u16x2(v[i].x & 0x7FFF7FFFu, v[i].y & 0x7FFF7FFFu),
+                          max_u16x2(v[i].z & 0x7FFF7FFFu, v[i].w & 0x7FFF7FFFu));
     }
+    // block 0's halves in the low 16 bits of both words, block 1's in the high ones
+    uint32_t m = max_u16x2(prmt(mx[0], mx[1], 0x5410u), prmt(mx[0], mx[1], 0x7632u));
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) m = max_u16x2(m, __shfl_xor_sync(0xffffffffu, m, off));
 
     uint32_t codes = 0;   // this lane's two UE8M0 bytes: block 2i + (lane >> 4) in byte i
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-        const int e = block_scale_exponent(amax[i] << 16);
+        const uint32_t amax = i == 0 ? (m & 0xFFFFu) : (m >> 16);
+        const int e = block_scale_exponent(amax << 16);
         if (valid[i]) codes |= static_cast<uint32_t>(e + 127) << (8 * i);
-        // 2^-e as FP32: e <= 120 for BF16 inputs (448 * 2^120 exceeds the BF16 maximum), so
-        // 127 - e >= 7 and the exponent field is a normal one.
-        const float s = __int_as_float((127 - e) << 23);
+        // 2^-e as a BF16 pair (e <= 120 for BF16 inputs, as 448 * 2^120 exceeds the BF16
+        // maximum, so 127 - e >= 7 and the exponent field is a normal one)
+        const uint32_t s2 = static_cast<uint32_t>(127 - e) * 0x00800080u;
         const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        uint32_t out[2] = {0u, 0u};
+        uint32_t c[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            // products by a power of two are exact (an FP32 underflow only hits values that
-            // round to zero in E4M3 anyway)
-            const float lo = __uint_as_float(w[j] << 16) * s;
-            const float hi = __uint_as_float(w[j] & 0xFFFF0000u) * s;
-            out[j >> 1] |= cvt_e4m3x2(lo, hi) << (16 * (j & 1));
+            const uint32_t y = mul_bf16x2(w[j], s2);
+            c[j] = cvt_e4m3x2(__uint_as_float(y << 16), __uint_as_float(y & 0xFFFF0000u));
         }
         if (valid[i])
-            *reinterpret_cast<uint2*>(q + row * K + 512 * kp + 256 * i + 8 * lane) = make_uint2(out[0], out[1]);
+            *reinterpret_cast<uint2*>(q + row * K + 512 * kp + 256 * i + 8 * lane) =
+                make_uint2(prmt(c[0], c[1], 0x5410u), prmt(c[2], c[3], 0x5410u));
     }
 
     // byte j of the word is block 4*kp + j: blocks 0 and 2 sit in lane 0, 1 and 3 in lane 16

@@ -18,7 +18,8 @@ pytestmark = pytest.mark.gpu
 
 CONFIGS = ["config_bn256_s4_a1", "config_bn224_s4_a2", "config_bn192_s5_a2", "config_bn128_s6_a2",
            "config_bn128_s4_a2", "config_bn64_s8_a2", "config_bn32_s8_a2", "config_bn224_s3_m2",
-           "config_bn192_s3_m2", "config_bn208_s3_m2", "config_bn128_s5_k2", "config_bn192_s5_k2"]
+           "config_bn192_s3_m2", "config_bn208_s3_m2", "config_bn128_s5_k2", "config_bn192_s5_k2",
+           "config_bn128_s8_k2_r64"]
 
 
 def _call_or_skip(fn, *args):
@@ -70,6 +71,46 @@ def test_split_k_decode_shape(split, monkeypatch):
     dg.dg_fp8_gemm_nt(to_dev(w["a"]), to_dev(sfa), to_dev(w["b"]), to_dev(sfb), d)
     dg.dg_check_device_error()
     assert_within_tolerance(bits(d), oracle.fp8_gemm_nt(w["a"], sfa, w["b"], sfb), f"decode split {split}")
+
+
+@pytest.mark.parametrize("M", [1, 37, 64])
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+def test_64_row_a_stages(M, split, few_sms, monkeypatch):
+    # The configuration that loads only 64 rows of A per stage (its MMAs still read 128 rows,
+    # the upper 64 from the next buffer): dense calls of at most 64 rows, on a few SMs so that
+    # each CTA (or cluster) walks many tiles, D pre-filled with a sentinel.
+    monkeypatch.setenv("DG_FORCE_CONFIG", "config_bn128_s8_k2_r64")
+    monkeypatch.setenv("DG_FORCE_SPLIT", str(split))
+    N, K = 704, 4608
+    w, sfa, sfb, want = _dense(M, N, K, seed=M + split)
+    d = torch.full((M, N), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
+    _call_or_skip(dg.dg_fp8_gemm_nt, to_dev(w["a"]), to_dev(sfa), to_dev(w["b"]), to_dev(sfb), d)
+    dg.dg_check_device_error()
+    assert_within_tolerance(bits(d), want, f"64-row A, M {M} split {split}")
+    # masked layout, groups of at most 64 rows
+    m = synth.make_masked(3, 64, 320, K, seed=M + 5 * split, masked_m=[64, 0, 17])
+    msfa = oracle.pack_sf_ue8m0(m["sfa"], 64, 1)
+    msfb = oracle.pack_sf_ue8m0(m["sfb"], 320, 128)
+    md = torch.full((3, 64, 320), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
+    _call_or_skip(dg.dg_m_grouped_fp8_gemm_nt_masked, to_dev(m["a"]), to_dev(msfa), to_dev(m["b"]), to_dev(msfb),
+                  md, to_dev(m["masked_m"]))
+    dg.dg_check_device_error()
+    prior = np.full((3, 64, 320), synth.SENTINEL_BF16, np.uint16)
+    wantm = oracle.m_grouped_fp8_gemm_nt_masked(m["a"], msfa, m["b"], msfb, m["masked_m"], prior)
+    got = bits(md)
+    rows = np.arange(64)[None, :] < m["masked_m"][:, None]
+    assert np.array_equal(got[~rows], wantm[~rows])
+    assert_within_tolerance(got[rows], wantm[rows], f"64-row A masked split {split}")
+
+
+def test_64_row_a_stages_refuse_taller_calls(monkeypatch):
+    # 65 rows of A do not fit 64-row stages: the forced plan is refused before any launch.
+    monkeypatch.setenv("DG_FORCE_CONFIG", "config_bn128_s8_k2_r64")
+    w, sfa, sfb, _ = _dense(65, 256, 512, seed=1)
+    d = torch.empty((65, 256), dtype=torch.int16, device="cuda")
+    with pytest.raises(dg.DGError) as e:
+        dg.dg_fp8_gemm_nt(to_dev(w["a"]), to_dev(sfa), to_dev(w["b"]), to_dev(sfb), d)
+    assert e.value.status == 2
 
 
 @pytest.mark.parametrize("cfg", ["config_bn128_s6_a2", "config_bn128_s4_a2", "config_bn64_s8_a2",

@@ -19,6 +19,8 @@ pytestmark = pytest.mark.gpu
 
 PLANS = [("config_bn128_s5_k2", 4), ("config_bn192_s5_k2", 1), ("config_bn128_s4_a2", 2),
          ("config_bn192_s5_a2", 1), ("config_bn64_s8_a2", 2)]
+# 64-row A stages take calls of at most 64 rows: the dense comparison (M = 64) only
+DENSE_PLANS = PLANS + [("config_bn128_s8_k2_r64", 1), ("config_bn128_s8_k2_r64", 4), ("config_bn128_s8_k2_r64", 8)]
 
 
 def _bf16_rne_bits(x):
@@ -36,7 +38,7 @@ def forced(monkeypatch):
     return setter
 
 
-@pytest.mark.parametrize("cfg,split", PLANS)
+@pytest.mark.parametrize("cfg,split", DENSE_PLANS)
 def test_dense_variant_matches_general_kernel(forced, cfg, split):
     forced(cfg, split)
     M, N, K = 64, 704, 2048
