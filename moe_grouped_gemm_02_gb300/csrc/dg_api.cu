@@ -418,15 +418,6 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     args.debug_drop_stage = -1;
     args.pdl = pdl_enabled();
     args.tma_store = plan.tma_store;
-    // Weights well inside L2 (decode and masked shapes): each CTA warms L2 with its first
-    // tile's B slice before waiting for the previous kernel (DG_PREFETCH_B=0 disables it).
-    {
-        const double b_bytes = static_cast<double>(b_groups) * N * static_cast<double>(K) * (call.b_fp4 ? 0.5 : 1.0);
-        const char* pf = std::getenv("DG_PREFETCH_B");
-        const bool pf_on = !(pf && pf[0] == '0');
-        args.prefetch_b = (pf_on && !call.b_mn && (mode == MODE_DENSE || mode == MODE_MASKED) &&
-                           b_bytes <= 64.0 * 1024 * 1024) ? 1 : 0;
-    }
     // D += A @ B^T in place: the epilogue's FP32 boxes are added to D by TMA reductions
     args.c_reduce = (call.out_f32 && call.c != nullptr && static_cast<const void*>(call.c) == call.d &&
                      plan.tma_store) ? 1 : 0;
@@ -453,6 +444,18 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
                      mode, groups, rows, N, K, call.a_mn, call.b_mn, call.out_f32, cfg->name, cfg->bn, cfg->stages,
                      cfg->acc, cfg->mh, plan.split, grid, args.raster_n);
     if (grid <= 0) return DG_OK;
+    // Dense GEMMs whose weights fit in L2 many times over and whose grid leaves at least half
+    // the SMs idle: each CTA warms L2 with its first tile's B slice and scale words before
+    // waiting for the previous kernel.  The next kernel's CTAs then start on the idle SMs
+    // while this one runs, and their prefetches overlap it; on a full grid the CTAs start only
+    // as the previous kernel's leave, and the prefetches measured slower (queued in front of
+    // the loads they were meant to warm).  DG_PREFETCH_B=0 / 1 forces it off / on.
+    {
+        const double b_bytes = static_cast<double>(b_groups) * N * static_cast<double>(K) * (call.b_fp4 ? 0.5 : 1.0);
+        const char* pf = std::getenv("DG_PREFETCH_B");
+        const bool eligible = !call.b_mn && mode == MODE_DENSE && b_bytes <= 64.0 * 1024 * 1024;
+        args.prefetch_b = eligible && (pf ? pf[0] == '1' : 2 * grid <= sms) ? 1 : 0;
+    }
     const cudaError_t e = cfg->launch(maps, args, grid, cs);
     return e == cudaSuccess ? DG_OK : cuda_fail("kernel launch", e);
 }

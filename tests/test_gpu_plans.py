@@ -73,20 +73,21 @@ def test_split_k_decode_shape(split, monkeypatch):
     assert_within_tolerance(bits(d), oracle.fp8_gemm_nt(w["a"], sfa, w["b"], sfb), f"decode split {split}")
 
 
+@pytest.mark.parametrize("cfg", ["config_bn128_s8_k2_r64"])
 @pytest.mark.parametrize("M", [1, 37, 64])
 @pytest.mark.parametrize("split", [1, 2, 4, 8])
-def test_64_row_a_stages(M, split, few_sms, monkeypatch):
-    # The configuration that loads only 64 rows of A per stage (its MMAs still read 128 rows,
+def test_64_row_a_stages(cfg, M, split, few_sms, monkeypatch):
+    # The configurations that load only 64 rows of A per stage (their MMAs still read 128 rows,
     # the upper 64 from the next buffer): dense calls of at most 64 rows, on a few SMs so that
     # each CTA (or cluster) walks many tiles, D pre-filled with a sentinel.
-    monkeypatch.setenv("DG_FORCE_CONFIG", "config_bn128_s8_k2_r64")
+    monkeypatch.setenv("DG_FORCE_CONFIG", cfg)
     monkeypatch.setenv("DG_FORCE_SPLIT", str(split))
     N, K = 704, 4608
     w, sfa, sfb, want = _dense(M, N, K, seed=M + split)
     d = torch.full((M, N), synth.SENTINEL_BF16, dtype=torch.int16, device="cuda")
     _call_or_skip(dg.dg_fp8_gemm_nt, to_dev(w["a"]), to_dev(sfa), to_dev(w["b"]), to_dev(sfb), d)
     dg.dg_check_device_error()
-    assert_within_tolerance(bits(d), want, f"64-row A, M {M} split {split}")
+    assert_within_tolerance(bits(d), want, f"64-row A {cfg}, M {M} split {split}")
     # masked layout, groups of at most 64 rows
     m = synth.make_masked(3, 64, 320, K, seed=M + 5 * split, masked_m=[64, 0, 17])
     msfa = oracle.pack_sf_ue8m0(m["sfa"], 64, 1)
@@ -100,7 +101,7 @@ def test_64_row_a_stages(M, split, few_sms, monkeypatch):
     got = bits(md)
     rows = np.arange(64)[None, :] < m["masked_m"][:, None]
     assert np.array_equal(got[~rows], wantm[~rows])
-    assert_within_tolerance(got[rows], wantm[rows], f"64-row A masked split {split}")
+    assert_within_tolerance(got[rows], wantm[rows], f"64-row A {cfg} masked split {split}")
 
 
 def test_64_row_a_stages_refuse_taller_calls(monkeypatch):
