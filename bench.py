@@ -633,7 +633,7 @@ def _random_e4m3(shape, gen, dev):
     return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)
 
 
-def time_next_rows(dev, peaks, reps: int = 20):
+def time_next_rows(dev, peaks, reps: int = 20, only: str | None = None):
     """Kernels timed beside the GEMM step, each alone on its own workload, L2 flushed before every
     rep: the per-token quantisation (algorithmic bytes = 2 MK read + MK codes + 4 Kp al4(M)
     scale bytes written), the K-grouped weight-gradient GEMM and the NN-layout FP32-accumulating
@@ -664,7 +664,12 @@ def time_next_rows(dev, peaks, reps: int = 20):
                 "frac": round(tf / fp8_peak, 4),
                 "peak_source": f"burst bf16 x {FP8_OVER_BF16:g} (of {peaks['source']})"}
 
+    def skip(name):
+        return only is not None and only not in name
+
     for name, M, K in NEXT_QUANTIZE:
+        if skip(name):
+            continue
         x = torch.randn((M, K), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
         q = torch.empty((M, K), dtype=torch.uint8, device=dev)
         sf = torch.empty(dg.packed_sf_shape(None, M, K), dtype=torch.int32, device=dev)
@@ -678,6 +683,21 @@ def time_next_rows(dev, peaks, reps: int = 20):
 
     # K-grouped weight gradient
     name, M, N = NEXT_K_GROUPED
+    if not skip(name):
+        _time_k_grouped(rows, name, M, N, gen, dev, stream, flush, reps, tensor_row)
+
+    # NN layout, FP32 out accumulated in place
+    name, M, N, K = NEXT_LAYOUT
+    if not skip(name):
+        _time_nn_layout(rows, name, M, N, K, gen, dev, stream, flush, reps, tensor_row)
+
+    _time_fp8_fp4(rows, gen, dev, stream, flush, reps, hbm_row, tensor_row, stream_row, skip)
+    return rows
+
+
+def _time_k_grouped(rows, name, M, N, gen, dev, stream, flush, reps, tensor_row):
+    """The K-grouped weight-gradient GEMM, D += A^T B in place (FP32)."""
+    import moe_grouped_gemm_02_gb300 as dg
     counts = synth.rng(0, "counts").multinomial(synth.CONTIGUOUS["tokens"], [0.25] * 4)
     ks = [synth.align_up(int(c), 128) for c in counts]
     sum_k = sum(ks)
@@ -696,10 +716,11 @@ def time_next_rows(dev, peaks, reps: int = 20):
     rows.append(tensor_row("K-grouped FP8 weight-gradient GEMM (dg_k_grouped_fp8_gemm_tn_contiguous), "
                            "D += A^T B in place", name, ms, lo, hi, 2.0 * M * N * sum_k,
                            sum_k * (M + N) + 2 * 4 * 4 * M * N))
-    del a, b, sfa, sfb, d
 
-    # NN layout, FP32 out accumulated in place
-    name, M, N, K = NEXT_LAYOUT
+
+def _time_nn_layout(rows, name, M, N, K, gen, dev, stream, flush, reps, tensor_row):
+    """The prefill shape in the NN layout, FP32 D += A B^T in place."""
+    import moe_grouped_gemm_02_gb300 as dg
     a = _random_e4m3((M, K), gen, dev)
     b = _random_e4m3((K, N), gen, dev)
     sfa = torch.full(dg.packed_sf_shape(None, M, K), 0x7F7F7F7F, dtype=torch.int32, device=dev)
@@ -712,14 +733,20 @@ def time_next_rows(dev, peaks, reps: int = 20):
     dg.dg_check_device_error()
     rows.append(tensor_row("FP8 GEMM, NN layout, D += A B^T in FP32 (dg_fp8_gemm)", name, ms, lo, hi,
                            2.0 * M * N * K, M * K + N * K + 2 * 4 * M * N))
-    del a, b, sfa, sfb, d
 
-    # FP8 x FP4: the decode shapes and the masked MoE shape with E2M1 weights (HBM-bound: the
-    # weights are read once at half the FP8 bytes), and the prefill shape (tensor-bound)
+
+def _time_fp8_fp4(rows, gen, dev, stream, flush, reps, hbm_row, tensor_row, stream_row, skip):
+    """FP8 x FP4: the decode shapes and the masked MoE shape with E2M1 weights (HBM-bound: the
+    weights are read once at half the FP8 bytes), and the prefill shape (tensor-bound)."""
+    import moe_grouped_gemm_02_gb300 as dg
+
     def fp4_weights(shape):
         return torch.randint(0, 256, shape, generator=gen, device=dev, dtype=torch.int32).to(torch.uint8)
 
     for (M, N, K) in synth.DECODE_SHAPES + [synth.PREFILL_SHAPE]:
+        name = f"fp8xfp4_{'prefill' if M == 4096 else 'decode'}_{M}x{N}x{K}"
+        if skip(name):
+            continue
         a = _random_e4m3((M, K), gen, dev)
         b = fp4_weights((N, K // 2))
         sfa = torch.full(dg.packed_sf_shape(None, M, K), 0x7F7F7F7F, dtype=torch.int32, device=dev)
@@ -730,7 +757,6 @@ def time_next_rows(dev, peaks, reps: int = 20):
             call()
         ms, lo, hi = _time_launches(call, stream, flush, reps)
         dg.dg_check_device_error()
-        name = f"fp8xfp4_{'prefill' if M == 4096 else 'decode'}_{M}x{N}x{K}"
         nbytes = M * K + N * K // 2 + 2 * M * N + 4 * (sfa.numel() + sfb.numel())
         row = "FP8 x FP4 GEMM (dg_fp8_fp4_gemm_nt)"
         if M == 4096:
@@ -742,8 +768,10 @@ def time_next_rows(dev, peaks, reps: int = 20):
             sms = _graph_stream_ms(lambda i, st: dg.dg_fp8_fp4_gemm_nt(a, sfa, bs[i], sfb, d, stream=st), copies)
             rows[-1].update(stream_row(sms, nbytes))
             del bs
-        del a, b, sfa, sfb, d
     G, max_m, N, K = (synth.MASKED[k] for k in ("G", "max_m", "N", "K"))
+    name = f"fp8xfp4_masked_{G}x{max_m}x{N}x{K}"
+    if skip(name):
+        return
     masked_m = synth.rng(0, "masked_m").integers(1, max_m + 1, size=G)
     a = _random_e4m3((G, max_m, K), gen, dev)
     b = fp4_weights((G, N, K // 2))
@@ -758,15 +786,14 @@ def time_next_rows(dev, peaks, reps: int = 20):
     dg.dg_check_device_error()
     valid = int(masked_m.sum())
     nbytes = valid * K + G * N * K // 2 + 2 * valid * N + 4 * (sfa.numel() + sfb.numel())
-    rows.append(hbm_row("FP8 x FP4 masked grouped GEMM (dg_m_grouped_fp8_fp4_gemm_nt_masked)",
-                        f"fp8xfp4_masked_{G}x{max_m}x{N}x{K}", ms, lo, hi, nbytes))
+    rows.append(hbm_row("FP8 x FP4 masked grouped GEMM (dg_m_grouped_fp8_fp4_gemm_nt_masked)", name, ms, lo, hi,
+                        nbytes))
     copies = _weight_copies(b.numel())
     bs = [b.clone() for _ in range(copies)]
     sms = _graph_stream_ms(lambda i, st: dg.dg_m_grouped_fp8_fp4_gemm_nt_masked(a, sfa, bs[i], sfb, d, mm, stream=st),
                            copies)
     rows[-1].update(stream_row(sms, nbytes))
     del bs
-    return rows
 
 
 def time_oracle(ws, budget_s: float = 20.0, rows_per_workload: int = 4):
@@ -847,6 +874,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the kernels timed beside the GEMM step")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
+    ap.add_argument("--next-only", default=None, metavar="NAME",
+                    help="time only the kernels beside the step whose workload name contains NAME (for "
+                         "profiling one kernel); prints their rows")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "dg":
         ap.error("--warmup must be at least 3")
@@ -859,6 +889,13 @@ def main():
             torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group(backend=backend)
     try:
+        if args.next_only is not None:
+            from moe_grouped_gemm_02_gb300 import build as dg_build
+            dg_build.build()
+            dev = torch.device("cuda", local_rank)
+            torch.cuda.set_device(dev)
+            print(json.dumps({"next_rows": time_next_rows(dev, read_peaks(), reps=5, only=args.next_only)}))
+            return
         out = run_reference(args, rank, world) if args.impl == "reference" else run_gpu(args, rank, world, local_rank)
         if rank == 0 and out is not None:
             print(json.dumps(out), flush=True)

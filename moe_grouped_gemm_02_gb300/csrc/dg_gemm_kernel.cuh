@@ -53,8 +53,6 @@ namespace dg {
 constexpr int BM = 128;       // rows per MMA: the tcgen05 M
 constexpr int BK = 128;       // K per stage: one 128-byte swizzle row, one scale block
 constexpr int MMA_K = 32;     // K of one kind::mxf8f6f4 MMA
-constexpr uint32_t SF_WARP = 6;      // warp that re-lays scale words for tcgen05.cp
-constexpr uint32_t MMA1_WARP = 7;    // second MMA issuer (MH = 2 or KS = 2)
 constexpr int DG_ERR_TIMEOUT_CODE = 6;
 
 template <int BN_, int STAGES_, int ACC_, int MH_ = 1, int KS_ = 1, int AR_ = 128>
@@ -71,10 +69,11 @@ struct GemmCfg {
     static constexpr int AR = AR_;
     static_assert(AR == 128 || (AR == 64 && MH_ == 1), "64-row A stages only with one 128-row half");
     // KS = 2: two MMA issuers split each 128-K stage (K steps 0-1 and 2-3) into the two TMEM
-    // accumulators, which the epilogue adds.  One thread issues at most one block-scaled MMA
-    // per ~161 cycles whatever its N, so for the narrow tiles of the HBM-bound shapes (N = 128,
-    // 192: 64-96 cycles of tensor work) a second issuer doubles the stage rate.  The two
-    // accumulators then serve one tile instead of alternating between tiles.
+    // accumulators, which the epilogue adds.  A block-scaled MMA occupies the tensor pipe for
+    // at least ~161 cycles whatever its N, so the narrow tiles of the HBM-bound shapes (N = 128,
+    // 192: 64-96 cycles of tensor work) take ~0.31 us per stage either way; the second issuer
+    // removes the issuing thread's own per-stage costs from that path (5-7 % faster decode
+    // GEMMs).  The two accumulators then serve one tile instead of alternating between tiles.
     static constexpr int KS = KS_;
     static constexpr int ISSUERS = MH * KS;
     static constexpr int ACC_ROT = KS == 2 ? 1 : ACC;   // accumulator sets rotated across tiles
@@ -86,6 +85,21 @@ struct GemmCfg {
     static constexpr int EPI_COLS = (MH == 1 && ACC_ == 1 && BN_ % 64 == 0) ? 2 : 1;
     static constexpr int THREADS = (MH == 2 || EPI_COLS == 2) ? 384 : (KS == 2 ? 256 : 224);
     static constexpr int EPI_THREADS = 128 * MH * EPI_COLS;
+    // Warp roles.  224/256 threads: producer 0, MMA issuer 1 (and 7 with KS = 2), epilogue 2-5,
+    // scale warp 6.  384 threads (two sets of epilogue warps): warpgroup 0 holds the producer
+    // (0), the issuers (1, and 3 with MH = 2) and the scale warp (2); warpgroups 1 and 2 the
+    // epilogue warps (4-7, 8-11).  Registers are then re-split per warpgroup (setmaxnreg):
+    // the launch gives every thread 168, warpgroup 0 drops to WG0_REGS and the epilogue
+    // warpgroups rise to EPI_REGS, which holds a 208-column BF16 row with no spills.
+    static constexpr bool WG_SPLIT = THREADS == 384;
+    static constexpr uint32_t SF_WARP = WG_SPLIT ? 2u : 6u;
+    static constexpr uint32_t MMA1_WARP = WG_SPLIT ? 3u : 7u;
+    static constexpr uint32_t EPI0 = WG_SPLIT ? 4u : 2u;     // first warp of epilogue set 0
+    static constexpr int LAUNCH_REGS = 168;                 // 65536 / 384, rounded down to 8
+    static constexpr int WG0_REGS = 64;
+    static constexpr int EPI_REGS = 216;
+    static_assert(!WG_SPLIT || 128 * WG0_REGS + 256 * EPI_REGS <= 384 * LAUNCH_REGS,
+                  "the re-split registers must fit the launch's allotment");
     static_assert(MH == 1 || MH == 2, "a tile has one or two 128-row halves");
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 16 in [32, 256]");
     // Accumulators start on 32-column boundaries: BN columns each, ACC_STRIDE apart.
@@ -264,7 +278,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmArgs& a, const int* cum, i
 
 // Bounded wait: true when the phase completed; false after the CTA aborted or this wait
 // timed out (then the error word and abort flag are set).
-static __device__ __noinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+__device__ __forceinline__ bool wait_or_abort_body(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                                   int* err, unsigned long long timeout_ns, int site) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
@@ -282,7 +296,7 @@ static __device__ __noinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 }
 
 // Same, acquiring at cluster scope: for barriers completed by other CTAs of the cluster.
-static __device__ __noinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+__device__ __forceinline__ bool wait_cluster_or_abort_body(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                                           int* err, unsigned long long timeout_ns, int site) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
@@ -299,9 +313,33 @@ static __device__ __noinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t
     }
 }
 
+// The bounded waits as out-of-line calls (a small main loop for the instruction cache), or
+// inlined (INL): the 384-thread kernels re-split registers per warpgroup, and a call there
+// would have to be compiled for every register count it is reached with.
+static __device__ __noinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                                  int* err, unsigned long long timeout_ns, int site) {
+    return wait_or_abort_body(bar, parity, abort_flag, err, timeout_ns, site);
+}
+static __device__ __noinline__ bool wait_cluster_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                                          int* err, unsigned long long timeout_ns, int site) {
+    return wait_cluster_or_abort_body(bar, parity, abort_flag, err, timeout_ns, site);
+}
+template <bool INL>
+__device__ __forceinline__ bool wait_or_abort_t(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, int* err,
+                                                unsigned long long timeout_ns, int site) {
+    if constexpr (INL) return wait_or_abort_body(bar, parity, abort_flag, err, timeout_ns, site);
+    else return wait_or_abort(bar, parity, abort_flag, err, timeout_ns, site);
+}
+template <bool INL>
+__device__ __forceinline__ bool wait_cluster_or_abort_t(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                                        int* err, unsigned long long timeout_ns, int site) {
+    if constexpr (INL) return wait_cluster_or_abort_body(bar, parity, abort_flag, err, timeout_ns, site);
+    else return wait_cluster_or_abort(bar, parity, abort_flag, err, timeout_ns, site);
+}
+template <bool INL>
 __device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag, int* err,
                                           unsigned long long timeout_ns, int site) {
-    return mbar_try_wait(bar, parity) || wait_or_abort(bar, parity, abort_flag, err, timeout_ns, site);
+    return mbar_try_wait(bar, parity) || wait_or_abort_t<INL>(bar, parity, abort_flag, err, timeout_ns, site);
 }
 
 // Re-lay one 128-row chunk of scale words (word r = row r, as TMA landed it) into the layout
@@ -544,7 +582,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // by the prefetch), so it overlaps the previous kernel: every thread that reads or writes
     // global memory waits for that kernel first, right before its first such access.
     griddep_launch_dependents();
-    if (args.mode == MODE_MASKED && warp == 2) {
+    if (args.mode == MODE_MASKED && warp == C::EPI0) {
         griddep_wait();
         // cum[g] = sum over g' < g of the m-units of group g' (128*MH-row tiles): each lane sums a contiguous run of groups, then an exclusive warp
         // scan over the runs.
@@ -570,7 +608,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         if (lane == 31) cum[G] = incl;
     }
-    if (args.mode == MODE_K_GROUPED && warp == 2) {
+    if (args.mode == MODE_K_GROUPED && warp == C::EPI0) {
         griddep_wait();
         // cum[g] = sum over g' < g of ks[g'] / 128 (K blocks) and cum[G + 1 + g] the same sum of
         // ceil(ks[g'] / 512) (packed scale-word rows): two exclusive warp scans over runs.
@@ -639,7 +677,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int kb0 = krank * args.kblocks / split;
     const int kb1 = (krank + 1) * args.kblocks / split;
 
+    // 384-thread kernels: warpgroup 0 (producer, issuers, scale warp) needs few registers, the
+    // epilogue warpgroups hold whole accumulator rows, so each role first moves registers from
+    // the first to the others (inside its own branch, so that the compiler allocates that
+    // role's code within the new count).  The host refuses to launch unless the kernel was
+    // given LAUNCH_REGS per thread, so the pool always holds what the increases ask for.
     if (warp == 0) {
+        if constexpr (C::WG_SPLIT) setmaxnreg_dec<C::WG0_REGS>();
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             int s = 0;
@@ -655,7 +699,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (t.zero) continue;
                 const int ga = args.mode == MODE_MASKED ? t.g : 0;
                 for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
-                    if (!wait_fast(empty_bar(s), ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_EMPTY)) {
+                    if (!wait_fast<C::WG_SPLIT>(empty_bar(s), ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_EMPTY)) {
                         ok = false;
                         break;
                     }
@@ -712,7 +756,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 }
             }
         }
-    } else if (warp == 1 || (C::ISSUERS == 2 && warp == MMA1_WARP)) {
+    } else if (warp == 1 || (C::ISSUERS == 2 && warp == C::MMA1_WARP)) {
+        if constexpr (C::WG_SPLIT) setmaxnreg_dec<C::WG0_REGS>();
         // ------------------------------------------------------------------ MMA issuer(s)
         // One lane per issuer, a minimal loop: the issuing thread's instruction stream is on
         // the critical path of the tensor pipe, so everything that can happen elsewhere does.
@@ -749,7 +794,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const Unit t = decode_unit<MH>(args, cum, u, kb0, kb1);
                 if (t.zero) continue;
                 const bool active = MH == 2 ? ((t.hmask >> h) & 1u) != 0u : (t.hmask & 1u) != 0u;
-                if (!wait_fast(tempty_bar(acc), acc_ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_TMEM_EMPTY)) {
+                if (!wait_fast<C::WG_SPLIT>(tempty_bar(acc), acc_ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_TMEM_EMPTY)) {
                     ok = false;
                     break;
                 }
@@ -760,7 +805,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         // First K block of a group (or of the range): copy the group's re-laid scale words from its
                         // ring slot into this issuer's TMEM slot.  (The slot's previous MMAs are
                         // complete: the producer waited for that before loading the slot.)
-                        if (!wait_fast(sfready_bar(sf_slot), (sfr_phbits >> sf_slot) & 1u, misc + 1, args.err,
+                        if (!wait_fast<C::WG_SPLIT>(sfready_bar(sf_slot), (sfr_phbits >> sf_slot) & 1u, misc + 1, args.err,
                                        args.timeout_ns, SITE_SF_READY)) {
                             ok = false;
                             break;
@@ -779,7 +824,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                                                                         sf_slot * C::SFB_BYTES + 512 * c));
                         }
                     }
-                    if (!wait_fast(full_bar(s), ph, misc + 1, args.err, args.timeout_ns, SITE_FULL)) {
+                    if (!wait_fast<C::WG_SPLIT>(full_bar(s), ph, misc + 1, args.err, args.timeout_ns, SITE_FULL)) {
                         ok = false;
                         break;
                     }
@@ -816,7 +861,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 while (!mbar_try_wait(last_bar, last_par) && global_timer_ns() - t0 < 100000000ull) {}
             }
         }
-    } else if (warp == SF_WARP) {
+    } else if (warp == C::SF_WARP) {
+        if constexpr (C::WG_SPLIT) setmaxnreg_dec<C::WG0_REGS>();
         // ------------------------------------------------------------------ scale re-layout
         // For every group of four K blocks, in order: wait for its scale words to land in their
         // ring slot, re-lay them for tcgen05.cp, publish them to the async proxy and signal the
@@ -840,7 +886,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int grp = t.kb_begin >> 2; grp <= (t.kb_end - 1) >> 2; ++grp) {
                 if (lane == 0) {
                     const uint32_t par = ((sfe_phbits >> sf_slot) & 1u) ^ 1u;
-                    if (wait_or_abort(sfempty_bar(sf_slot), par, misc + 1, args.err, args.timeout_ns, SITE_SF_EMPTY)) {
+                    if (wait_or_abort_t<C::WG_SPLIT>(sfempty_bar(sf_slot), par, misc + 1, args.err, args.timeout_ns, SITE_SF_EMPTY)) {
                         const uint32_t sb = sffull_bar(sf_slot);
                         mbar_arrive_expect_tx(sb, C::TX_SF);
                         const int kp = t.kpoff + grp;
@@ -860,7 +906,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     ok = false;
                     break;
                 }
-                if (!wait_fast(sffull_bar(sf_slot), (sff_phbits >> sf_slot) & 1u, misc + 1, args.err,
+                if (!wait_fast<C::WG_SPLIT>(sffull_bar(sf_slot), (sff_phbits >> sf_slot) & 1u, misc + 1, args.err,
                                args.timeout_ns, SITE_SF_FULL)) {
                     ok = false;
                     break;
@@ -883,7 +929,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(sffull_bar(sf_last), sf_last_par) && global_timer_ns() - t0 < 100000000ull) {}
         }
-    } else if ((warp >= 2 && warp <= 5) || ((MH == 2 || C::EPI_COLS == 2) && warp >= 8)) {
+    } else if (C::WG_SPLIT && C::ISSUERS == 1 && warp == 3) {
+        // warpgroup 0's spare warp (one issuer): it takes part in the warpgroup's re-split only
+        setmaxnreg_dec<C::WG0_REGS>();
+    } else if ((warp >= C::EPI0 && warp < C::EPI0 + 4u) || ((MH == 2 || C::EPI_COLS == 2) && warp >= 8)) {
+        if constexpr (C::WG_SPLIT) setmaxnreg_inc<C::EPI_REGS>();
         // ------------------------------------------------------------------ epilogue
         // Warps 2-5 write half 0 of each tile, warps 8-11 half 1 (MH = 2) or the second half of
         // the columns (EPI_COLS = 2).
@@ -898,7 +948,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // loaded on the box path, and a tile with nothing computed leaves D as it is.
         const bool c_red = use_c && args.c_reduce != 0;
         // This warp's two 1 KB output staging buffers (no split-K: the receive region is free).
-        const uint32_t ew = warp <= 5 ? warp - 2u : warp - 4u;     // epilogue warp index 0..7
+        const uint32_t ew = warp < 8 ? warp - C::EPI0 : warp - 4u;   // epilogue warp index 0..7
         const uint32_t stage_out = base + C::off_stage_out(extra_smem_ints(args.mode, args.groups)) + ew * 2048u;
         uint32_t nbox = 0;                                          // boxes this warp has stored
         const int row_in_half = static_cast<int>(q * 32 + lane);
@@ -972,14 +1022,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     if (recv_lane && write) store_zero_row(args, row_off, n0, min(N, n0 + C::BN));
                     continue;
                 }
-                if (!wait_or_abort(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
+                if (!wait_or_abort_t<C::WG_SPLIT>(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
                 tc_fence_after_sync();
                 const uint32_t t_row = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * C::ACC_STRIDE);
                 // the other CTAs are done with the previous unit's receive slots
                 bool slots_free = true;
                 for (uint32_t o = 0; o < usplit && slots_free; ++o)
                     if (o != crank)
-                        slots_free = wait_cluster_or_abort(slotfree_bar(o), red_eph ^ 1u, misc + 1, args.err,
+                        slots_free = wait_cluster_or_abort_t<C::WG_SPLIT>(slotfree_bar(o), red_eph ^ 1u, misc + 1, args.err,
                                                            args.timeout_ns, SITE_RED_EMPTY);
                 if (!slots_free) break;
                 red_eph ^= 1u;
@@ -1038,11 +1088,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     // others in rank order.
                     __syncwarp();
                     if (lane == 0) mbar_arrive(unitdone_bar);
-                    if (!wait_or_abort(unitdone_bar, red_dph, misc + 1, args.err, args.timeout_ns, SITE_RED_UNIT)) break;
+                    if (!wait_or_abort_t<C::WG_SPLIT>(unitdone_bar, red_dph, misc + 1, args.err, args.timeout_ns, SITE_RED_UNIT)) break;
                     red_dph ^= 1u;
                     bool landed = true;
                     for (uint32_t qq = qr0; qq < qr1 && landed; ++qq)
-                        landed = wait_cluster_or_abort(redfull_bar(static_cast<int>(qq)), (red_fmask >> qq) & 1u,
+                        landed = wait_cluster_or_abort_t<C::WG_SPLIT>(redfull_bar(static_cast<int>(qq)), (red_fmask >> qq) & 1u,
                                                        misc + 1, args.err, args.timeout_ns, SITE_RED_FULL);
                     if (!landed) break;
                     for (uint32_t qq = qr0; qq < qr1; ++qq) red_fmask ^= 1u << qq;
@@ -1052,7 +1102,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     cluster_arrive();
                     final_arrived = true;
                     constexpr uint32_t UPR = C::BN / 8;               // 16-byte units per row
-                    const uint32_t et = (warp - 2u) * 32u + lane;     // epilogue thread 0..127
+                    const uint32_t et = (warp - C::EPI0) * 32u + lane;  // epilogue thread 0..127
                     for (uint32_t i = et; i < (own1 - own0) * UPR; i += static_cast<uint32_t>(C::EPI_THREADS)) {
                         const uint32_t rr = i / UPR, off = 32u * (i - rr * UPR);
                         uint32_t r[32];
@@ -1108,7 +1158,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         mbar_arrive_expect_tx(redfull_bar(static_cast<int>(q)),
                                               (usplit - 1u) * (ro1 - ro0) * static_cast<uint32_t>(C::BN * 4));
                     __syncwarp();
-                    if (!wait_cluster_or_abort(redfull_bar(static_cast<int>(q)), (red_fmask >> q) & 1u, misc + 1,
+                    if (!wait_cluster_or_abort_t<C::WG_SPLIT>(redfull_bar(static_cast<int>(q)), (red_fmask >> q) & 1u, misc + 1,
                                                args.err, args.timeout_ns, SITE_RED_FULL))
                         break;
                     const uint32_t src = recv_base + (recv_lane ? r_in_tile - own0 : 0u) * C::RECV_ROW;
@@ -1152,9 +1202,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 // keeps every CTA's shared memory alive until the peers' copies have landed).
                 __syncwarp();
                 if (lane == 0) mbar_arrive(unitdone_bar);
-                if (!wait_or_abort(unitdone_bar, red_dph, misc + 1, args.err, args.timeout_ns, SITE_RED_UNIT)) break;
+                if (!wait_or_abort_t<C::WG_SPLIT>(unitdone_bar, red_dph, misc + 1, args.err, args.timeout_ns, SITE_RED_UNIT)) break;
                 red_dph ^= 1u;
-                if (warp == 2 && lane == 0)
+                if (warp == C::EPI0 && lane == 0)
                     for (uint32_t rk = 0; rk < usplit; ++rk)
                         if (rk != crank) mbar_arrive_remote(map_to_rank(slotfree_bar(crank), rk));
                 continue;
@@ -1181,7 +1231,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     load_c_chunk(args, roff_of(row), c0, N, 32, cv_next);
                 }
             }
-            if (!wait_or_abort(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
+            if (!wait_or_abort_t<C::WG_SPLIT>(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
             tc_fence_after_sync();
             {
                 const int h = my_half;
@@ -1227,10 +1277,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     static_assert(C::BN % (16 * C::EPI_COLS) == 0, "whole 16-column pieces per epilogue warp");
                     const int pc0 = 2 * ch_lo;                   // first piece of this thread's segment
                     uint32_t pk[NP * 8];
-                    // 32 columns per TMEM load (half the round trips) where registers allow: with
-                    // 384 threads a thread has at most 168, and K-split kernels load two
-                    // accumulators, so those with more than 128 columns load 16 at a time.
-                    constexpr int LDC = (C::THREADS <= 256 && (C::KS == 1 || C::BN <= 128)) ? 32 : 16;
+                    // 32 columns per TMEM load (half the round trips) where registers allow: K-split
+                    // kernels load two accumulators, so those with more than 128 columns load 16 at
+                    // a time (the 384-thread kernels' epilogue warps have EPI_REGS registers).
+                    constexpr int LDC = ((C::THREADS <= 256 && (C::KS == 1 || C::BN <= 128)) || C::WG_SPLIT) ? 32 : 16;
                     auto load_pieces = [&](int i, auto width) {   // pieces i (and i + 1 when 32 wide)
                         uint32_t r[32];
                         const uint32_t col = t_row + 16u * static_cast<uint32_t>(pc0 + i);
@@ -1466,6 +1516,14 @@ int max_clusters_fp8_gemm(int cluster, size_t smem) {
 template <class C>
 cudaError_t prepare_fp8_gemm(int max_smem) {
     auto prep = [&](auto kernel) {
+        if (C::WG_SPLIT) {
+            // The per-warpgroup register re-split draws on the registers the launch gives every
+            // thread: with fewer, the epilogue's increase could never be granted.
+            cudaFuncAttributes fa;
+            const cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs < C::LAUNCH_REGS) return cudaErrorInvalidConfiguration;
+        }
         return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     };
     cudaError_t e = prep(fp8_gemm_kernel<C, SPEC_ANY>);

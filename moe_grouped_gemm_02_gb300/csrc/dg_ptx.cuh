@@ -151,6 +151,21 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
 }
 
 // ---------------------------------------------------------------------------------------
+// Per-warpgroup register re-split (all four warps of a warpgroup execute the same one)
+// ---------------------------------------------------------------------------------------
+// Lower this warpgroup's registers per thread to N, returning the rest to the CTA's pool.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+// Raise this warpgroup's registers per thread to N, taking them from the CTA's pool (waits
+// until the pool holds them).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------------------
 // Fences
 // ---------------------------------------------------------------------------------------
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA, tcgen05).
