@@ -44,10 +44,47 @@ __global__ void __launch_bounds__(256) pack_sf_kernel(const float* __restrict__ 
     out[(static_cast<size_t>(g) * Kp + kp) * mn_al + r] = static_cast<int32_t>(w);
 }
 
+// Per-row scales (gran_mn = 1, the activations' scales packed every step): the pack is a
+// transpose, [row][K block] floats to [word][row] words.  Each CTA stages a tile of PACK_ROWS
+// rows x PACK_WORDS words (32 K blocks) through shared memory: a warp loads one row's 32
+// scales per instruction (128 contiguous bytes), each becomes one UE8M0 byte of a row-major
+// byte tile, then the words go out along the rows (coalesced).  Tile rows are padded to an odd
+// number of words, so the word reads of consecutive rows fall in distinct banks.
+constexpr int PACK_ROWS = 64;
+constexpr int PACK_WORDS = 8;
+constexpr int PACK_STRIDE = PACK_WORDS + 1;   // words per tile row
+
+__global__ void __launch_bounds__(256) pack_sf_rows_kernel(const float* __restrict__ sf, int32_t* __restrict__ out,
+                                                           int MN, int Kb, int Kp, int mn_al) {
+    __shared__ uint32_t tile[PACK_ROWS * PACK_STRIDE];
+    griddep_wait();
+    griddep_launch_dependents();
+    const int r0 = blockIdx.x * PACK_ROWS;
+    const int kp0 = blockIdx.y * PACK_WORDS;
+    const int g = blockIdx.z;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    uint8_t* bytes = reinterpret_cast<uint8_t*>(tile);
+    const int kb = 4 * kp0 + lane;
+    // warp w takes rows w, w + 8, ...: one 32-scale row segment per load, all in flight at once
+#pragma unroll
+    for (int r = warp; r < PACK_ROWS; r += 8) {
+        const int row = r0 + r;
+        uint32_t code = 0u;
+        if (row < MN && kb < Kb) code = ue8m0_code_ceil(__ldg(sf + (static_cast<size_t>(g) * MN + row) * Kb + kb));
+        bytes[r * 4 * PACK_STRIDE + lane] = static_cast<uint8_t>(code);
+    }
+    __syncthreads();
+    // word kp of row r: bytes 4kp..4kp+3 of the row (little-endian: K block 4kp in byte 0)
+    for (int i = threadIdx.x; i < PACK_ROWS * PACK_WORDS; i += blockDim.x) {
+        const int w = i / PACK_ROWS, r = i - w * PACK_ROWS;
+        if (kp0 + w < Kp && r0 + r < mn_al)
+            out[(static_cast<size_t>(g) * Kp + kp0 + w) * mn_al + r0 + r] = static_cast<int32_t>(tile[r * PACK_STRIDE + w]);
+    }
+}
+
 cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb, int Kb, int Kp,
                            int mn_al, int gran_mn, int pdl, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((mn_al + 255) / 256, Kp, G);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -55,6 +92,11 @@ cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    if (gran_mn == 1) {
+        cfg.gridDim = dim3((mn_al + PACK_ROWS - 1) / PACK_ROWS, (Kp + PACK_WORDS - 1) / PACK_WORDS, G);
+        return cudaLaunchKernelEx(&cfg, pack_sf_rows_kernel, sf, out, MN, Kb, Kp, mn_al);
+    }
+    cfg.gridDim = dim3((mn_al + 255) / 256, Kp, G);
     return cudaLaunchKernelEx(&cfg, pack_sf_kernel, sf, out, MN, MNb, Kb, Kp, mn_al, gran_mn);
 }
 

@@ -20,7 +20,9 @@ def _gpu_pack(sf: np.ndarray, mn: int, gran: int) -> np.ndarray:
 
 
 @pytest.mark.parametrize("G,MN,gran,Kb", [(1, 128, 1, 8), (1, 5, 1, 5), (2, 4096, 1, 56), (4, 130, 128, 9),
-                                          (3, 7168, 128, 16), (1, 1, 1, 1), (2, 2112, 128, 56), (1, 33, 1, 3)])
+                                          (3, 7168, 128, 16), (1, 1, 1, 1), (2, 2112, 128, 56), (1, 33, 1, 3),
+                                          (3, 257, 1, 17),     # partial last tile of 128 rows, odd word count
+                                          (1, 70, 1, 400)])    # 100 words per row: 13 word tiles, the last partial
 def test_pack_powers_of_two(G, MN, gran, Kb):
     rs = np.random.default_rng(G * 1000 + MN + Kb)
     MNb = -(-MN // gran)
