@@ -583,6 +583,42 @@ def time_hbm_streams(ws, dws, per_wl, peaks):
     dg.dg_check_device_error()
 
 
+def run_workload_only(args, local_rank: int):
+    """One workload of the suite alone: its weights' scales packed once, then `warmup` untimed and
+    `steps` timed launches of (activation-scale pack + GEMM), the GEMM bracketed by CUDA events
+    with L2 flushed before each launch.  For profiling one kernel on its full-size workload."""
+    from moe_grouped_gemm_02_gb300 import build as dg_build
+    import moe_grouped_gemm_02_gb300 as dg
+    dg_build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    ws = [w for w in make_workloads(seed=0) if args.workload_only in w["name"]]
+    if not ws:
+        raise SystemExit(f"no workload matches {args.workload_only!r}")
+    w = ws[0]
+    dw = DeviceWorkload(w, dev)
+    dw.pack_weights()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        dw.pack()
+        dw.gemm()
+    ts = []
+    for r in range(args.steps):
+        flush.fill_(float(r))
+        dw.pack()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dw.gemm()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    dg.dg_check_device_error()
+    ms = statistics.median(ts)
+    return {"workload": w["name"], "launches": args.steps, "ms": round(ms, 5), "ms_min": round(min(ts), 5),
+            "tflops": round(w["flops"] / (ms * 1e-3) / 1e12, 1), "gbs": round(w["bytes"] / (ms * 1e-3) / 1e9, 1)}
+
+
 def time_small_dense(dev, peaks, reps: int = 20):
     """The small dense GEMM 128x512x1024 (A, B ~ N(0, 1), seed 0), timed beside the step as a
     latency-bound row of its own: bracketed alone with L2 flushed before each rep, and back to
@@ -874,6 +910,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip the kernels timed beside the GEMM step")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
+    ap.add_argument("--workload-only", default=None, metavar="NAME",
+                    help="set up only the suite workload whose name contains NAME and time its GEMM alone "
+                         "(activation-scale pack + GEMM per launch, L2 flushed before each); prints one line")
     ap.add_argument("--next-only", default=None, metavar="NAME",
                     help="time only the kernels beside the step whose workload name contains NAME (for "
                          "profiling one kernel); prints their rows")
@@ -889,6 +928,9 @@ def main():
             torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group(backend=backend)
     try:
+        if args.workload_only is not None:
+            print(json.dumps(run_workload_only(args, local_rank)))
+            return
         if args.next_only is not None:
             from moe_grouped_gemm_02_gb300 import build as dg_build
             dg_build.build()
