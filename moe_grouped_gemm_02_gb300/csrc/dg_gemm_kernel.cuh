@@ -155,6 +155,11 @@ struct GemmCfg {
     static __host__ __device__ uint32_t off_stage_out(int extra_ints) {
         return (static_cast<uint32_t>(OFF_CUM + extra_ints * 4) + 1023u) & ~1023u;
     }
+    // Whether any split-K launch of this configuration fits in a CTA's shared memory (227 KB at
+    // most on this architecture): if not, the kernel is built without the split-K code.
+    static constexpr bool SPLITK_POSSIBLE =
+        MH == 1 && EPI_COLS == 1 &&
+        1024 + ((OFF_CUM + 15) & ~15) + (AR / 2) * RECV_ROW <= 227 * 1024;
     static size_t smem_bytes(int extra_ints, int split, int tma_store) {
         if (split > 1) return 1024 + off_recv(extra_ints) + recv_bytes(split);
         return 1024 + (tma_store ? off_stage_out(extra_ints) + STAGE_OUT_BYTES : off_recv(extra_ints));
@@ -503,7 +508,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     auto redfull_bar = [&](int j) { return base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + j); };
     auto slotfree_bar = [&](uint32_t o) { return base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + 4 + o); };
     const uint32_t unitdone_bar = base + C::OFF_BAR + 8u * (SFB0 + 3 * C::SF_SLOTS + 12);
-    const int split = (MH == 1 && C::EPI_COLS == 1) ? args.split : 1;
+    const int split = C::SPLITK_POSSIBLE ? args.split : 1;
     const uint32_t recv_base = base + C::off_recv(extra_smem_ints(args.mode, args.groups));
 
     if (threadIdx.x == 0) {

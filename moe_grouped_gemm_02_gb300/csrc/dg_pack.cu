@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(256) pack_sf_kernel(const float* __restrict__ 
     out[(static_cast<size_t>(g) * Kp + kp) * mn_al + r] = static_cast<int32_t>(w);
 }
 
-// Per-row scales (gran_mn = 1, the activations' scales packed every step): the pack is a
+// Per-row scales of more than 256 rows (gran_mn = 1, the activations' scales packed every step): the pack is a
 // transpose, [row][K block] floats to [word][row] words.  Each CTA stages a tile of PACK_ROWS
 // rows x PACK_WORDS words (32 K blocks) through shared memory: a warp loads one row's 32
 // scales per instruction (128 contiguous bytes), each becomes one UE8M0 byte of a row-major
@@ -92,7 +92,9 @@ cudaError_t launch_pack_sf(const float* sf, int32_t* out, int G, int MN, int MNb
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (gran_mn == 1) {
+    // (a few hundred rows leave the tiled kernel with too few CTAs to hide the load latency:
+    // there one thread per word, Kp CTAs per 256 rows, is faster)
+    if (gran_mn == 1 && MN > 256) {
         cfg.gridDim = dim3((mn_al + PACK_ROWS - 1) / PACK_ROWS, (Kp + PACK_WORDS - 1) / PACK_WORDS, G);
         return cudaLaunchKernelEx(&cfg, pack_sf_rows_kernel, sf, out, MN, Kb, Kp, mn_al);
     }
