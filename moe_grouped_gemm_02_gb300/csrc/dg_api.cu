@@ -351,7 +351,7 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     if (!plan.cfg) return DG_ERR_SHAPE;   // nothing fits in shared memory (too many groups)
     const KernelConfig* cfg = plan.cfg;
 
-    CUtensorMap maps[5];
+    CUtensorMap maps[6];
     // A and D have one group per masked group; B one per expert (contiguous, masked).  K-grouped
     // operands are single [sum K, MN] matrices whose groups are K ranges.
     const int a_groups = mode == MODE_MASKED ? groups : 1;
@@ -386,6 +386,11 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
                                              16, 32, CU_TENSOR_MAP_SWIZZLE_NONE));
     else
         maps[4] = maps[0];   // unused
+    if (plan.tma_store && !call.out_f32)
+        ok = ok && encode_3d(&maps[5], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, call.d, N, rows, d_groups, 64, 32,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        maps[5] = maps[0];   // unused
     if (!ok) return cuda_fail("cuTensorMapEncodeTiled", cudaErrorInvalidValue);
 
     GemmArgs args{};

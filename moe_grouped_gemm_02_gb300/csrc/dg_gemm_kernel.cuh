@@ -472,7 +472,8 @@ template <class C, int SPEC>
 __global__ void __launch_bounds__(C::THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
-                    const __grid_constant__ CUtensorMap tm_d, const GemmArgs args_in) {
+                    const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_d64,
+                    const GemmArgs args_in) {
     GemmArgs args = args_in;
     if (SPEC != SPEC_ANY) {
         const bool dense = SPEC == SPEC_DENSE || SPEC == SPEC_DENSE_FP4;
@@ -538,7 +539,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         fence_mbarrier_init();
     }
     if (warp == 0 && lane == 0) {
-        if (args.tma_store) tma_prefetch_desc(&tm_d);
+        if (args.tma_store) {
+            tma_prefetch_desc(&tm_d);
+            if (C::ACC == 2 && !args.out_f32) tma_prefetch_desc(&tm_d64);
+        }
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
         tma_prefetch_desc(&tm_sfa);
@@ -1315,6 +1319,38 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     // 16-byte unit j of slab row r sits at unit j ^ ((r >> 1) & 3) of the row's 64
                     // bytes, which keeps both the writes and the reads free of bank conflicts.
                     int i_direct = 0;    // first piece stored row by row
+                    // On the CTA's last unit the operand ring is idle (every stage was consumed by
+                    // MMAs that have completed): the warp stages its 32 rows x BN of BF16 there as
+                    // 64-column boxes in the 128-byte swizzled layout (16-byte unit j of row r at
+                    // unit j ^ (r mod 8): conflict-free writes) and one lane writes them out with
+                    // one TMA bulk store per box.  The CTA may leave as soon as the TMA has read
+                    // them, instead of after a chain of row stores.  Masked slabs that reach past
+                    // masked_m keep the row stores below (rows past it stay untouched).
+                    const bool last_unit_here = u + u_step >= total_units;
+                    if (C::ACC == 2 && args.tma_store && slab_tma && last_unit_here && C::BN % 64 == 0) {
+                        const uint32_t region = base + C::OFF_A + ew * static_cast<uint32_t>(32 * C::BN * 2);
+                        const uint32_t rsw = lane & 7u;
+#pragma unroll
+                        for (int b = 0; b < C::BN / 64; ++b) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const uint32_t* p = pk + 8 * (4 * b + j / 2) + 4 * (j % 2);
+                                st_shared_v4(region + static_cast<uint32_t>(b) * 4096u + lane * 128u +
+                                                 16u * (static_cast<uint32_t>(j) ^ rsw),
+                                             make_uint4(p[0], p[1], p[2], p[3]));
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            for (int b = 0; b < C::BN / 64; ++b)
+                                if (n0 + 64 * b < N)
+                                    tma_store_3d(&tm_d64, region + static_cast<uint32_t>(b) * 4096u, n0 + 64 * b, slab0, t.g);
+                            bulk_commit_group();
+                        }
+                        ++nbox;
+                        continue;   // the accumulator was released above
+                    }
                     if (C::ACC == 2 && args.tma_store) {
                         uint16_t* dgrp = static_cast<uint16_t*>(args.d) +
                                          static_cast<size_t>(t.g) * args.rows * static_cast<size_t>(N);
@@ -1431,7 +1467,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             mbar_arrive(tempty_bar(acc));
             if (++acc == C::ACC_ROT) { acc = 0; acc_ph ^= 1u; }
         }
-        if (lane == 0 && nbox > 0) bulk_wait_group_all();   // D is written before the CTA ends
+        // The CTA's shared memory must outlive the bulk stores' reads of it (their writes to D
+        // complete on their own before the grid does).
+        if (lane == 0 && nbox > 0) bulk_wait_group_read<0>();
         __syncwarp();
         if (final_arrived) {
             // the final barrier: this warp arrived early; wait with everyone else
@@ -1485,7 +1523,7 @@ cudaError_t launch_fp8_gemm(const CUtensorMap* maps, const GemmArgs& args, int g
                      : args.mode == MODE_MASKED ? (args.b_fp4 ? SPEC_MASKED_FP4 : SPEC_MASKED)
                                                 : SPEC_ANY;
     auto launch = [&](auto kernel) {
-        return cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], maps[2], maps[3], maps[4], args);
+        return cudaLaunchKernelEx(&cfg, kernel, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], args);
     };
     constexpr bool V = C::MH == 1;   // 256-row configurations have only the general kernel
     switch (spec) {

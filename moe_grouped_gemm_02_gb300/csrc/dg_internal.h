@@ -54,7 +54,8 @@ __host__ __device__ inline int extra_smem_ints(int mode, int groups) {
     return mode == MODE_MASKED ? groups + 1 : (mode == MODE_K_GROUPED ? 2 * (groups + 1) : 0);
 }
 
-// maps: A, B, scales of A, scales of B, D
+// maps: A, B, scales of A, scales of B, D (32 x 32-byte boxes), D (BF16: 64-column x 32-row
+// boxes in the 128-byte swizzle, for whole-tile stores from the idle operand ring)
 using GemmLaunchFn = cudaError_t (*)(const CUtensorMap* maps, const GemmArgs& args, int grid,
                                      cudaStream_t stream);
 
