@@ -423,6 +423,15 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     args.debug_drop_stage = -1;
     args.pdl = pdl_enabled();
     args.tma_store = plan.tma_store;
+    // An output larger than L2 cannot stay there for whoever reads it next: its stores are
+    // marked evict-first, so that they do not evict the weight tiles the kernel re-reads
+    // (DG_D_EVICT_FIRST=0 disables it).
+    {
+        const double d_bytes = static_cast<double>(rows) * N * (call.out_f32 ? 4.0 : 2.0) *
+                               ((mode == MODE_MASKED || mode == MODE_K_GROUPED) ? groups : 1);
+        const char* ef = std::getenv("DG_D_EVICT_FIRST");
+        args.d_evict_first = (!(ef && ef[0] == '0') && d_bytes > 128.0 * 1024 * 1024) ? 1 : 0;
+    }
     // D += A @ B^T in place: the epilogue's FP32 boxes are added to D by TMA reductions
     args.c_reduce = (call.out_f32 && call.c != nullptr && static_cast<const void*>(call.c) == call.d &&
                      plan.tma_store) ? 1 : 0;

@@ -1271,6 +1271,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     __syncwarp();
                     if (lane == 0) {
                         if (c_red) tma_reduce_add_3d(&tm_d, buf, col, slab0, t.g);
+                        else if (args.d_evict_first) tma_store_3d_hint(&tm_d, buf, col, slab0, t.g, l2_policy_evict_first());
                         else tma_store_3d(&tm_d, buf, col, slab0, t.g);
                         bulk_commit_group();
                     }

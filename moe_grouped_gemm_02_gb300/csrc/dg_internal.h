@@ -44,6 +44,8 @@ struct GemmArgs {
     int tma_store;          // the epilogue writes D through its tensor map (else plain stores)
     int prefetch_b;         // before its dependency wait, each CTA prefetches its first tile's B slice
                             // into L2 (weights that fit in L2 many times over)
+    int d_evict_first;      // D is larger than L2: its TMA stores carry an L2 evict-first hint so that
+                            // they do not push the operand tiles still being re-read out of L2
     int c_reduce;           // FP32 C is D itself and D goes out through its tensor map: the epilogue's
                             // boxes are added to D in place by TMA reductions (no C loads)
 };

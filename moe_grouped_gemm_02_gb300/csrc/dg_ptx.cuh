@@ -237,6 +237,20 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
                  "r"(x), "r"(y), "r"(z), "r"(src)
                  : "memory");
 }
+// The same store with an L2 cache-eviction policy (`policy` from l2_policy_evict_first).
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y, int32_t z,
+                                                  uint64_t policy) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(src), "l"(policy)
+                 : "memory");
+}
+// An L2 policy under which the lines it covers are the first to be evicted.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's bulk groups still read their shared-memory source.
 template <int N>
