@@ -42,6 +42,11 @@
  *    DG_TIMEOUT_MS sets the bound on each in-kernel barrier wait (default 4000) and
  *    DG_DEBUG_DROP_LOAD=n makes the GEMM skip its n-th load stage, so that a wait runs out:
  *    a test hook for the timeout path (dg_check_device_error then reports DG_ERR_TIMEOUT).
+ *    Two performance switches, neither of which changes a result: DG_PREFETCH_B=0 / 1 turns
+ *    off / forces the L2 prefetch of a dense GEMM's weight tiles before it waits for the
+ *    previous kernel (by default on for weights of at most 64 MB whose grid leaves half the
+ *    SMs idle); DG_D_EVICT_FIRST=0 stores an output larger than the L2 without the
+ *    evict-first cache hint (by default the hint is on for outputs above 128 MB).
  */
 #ifndef DG_H
 #define DG_H
