@@ -122,6 +122,20 @@ __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Whole warp: true in one lane (the lowest active one), false in the others.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t elected;
+    asm volatile(
+        "{\n"
+        "  .reg .pred p;\n"
+        "  .reg .b32 lane;\n"
+        "  elect.sync lane|p, 0xffffffff;\n"
+        "  selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(elected));
+    return elected != 0;
+}
+
 // Named CTA barrier `id` over `count` threads: arrive without waiting, or arrive and wait.
 __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
