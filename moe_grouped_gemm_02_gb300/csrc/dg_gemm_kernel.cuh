@@ -701,7 +701,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     if (warp == 0) {
         if constexpr (C::WG_SPLIT) setmaxnreg_dec<C::WG0_REGS>();
         // ------------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        // Like the MMA issuers: the whole warp walks the loop and waits, one elected lane arms
+        // the barriers and issues the loads.
+        const bool leader = elect_one_sync();
+        {
             int s = 0;
             uint32_t ph = 0;
             uint32_t issued = 0;   // stages issued in total (for the abort drain)
@@ -715,7 +718,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (t.zero) continue;
                 const int ga = args.mode == MODE_MASKED ? t.g : 0;
                 for (int kb = t.kb_begin; kb < t.kb_end; ++kb) {
-                    if (!wait_fast<C::WG_SPLIT>(empty_bar(s), ph ^ 1u, misc + 1, args.err, args.timeout_ns, SITE_EMPTY)) {
+                    if (!wait_fast_warp<C::WG_SPLIT>(empty_bar(s), ph ^ 1u, misc + 1, args.err, args.timeout_ns,
+                                                     SITE_EMPTY)) {
                         ok = false;
                         break;
                     }
@@ -726,36 +730,40 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         if (++s == C::STAGES) { s = 0; ph ^= 1u; }
                         continue;
                     }
-                    const uint32_t fb = full_bar(s);
-                    // An unpacking E2M1 load counts the packed bytes it reads (half its shared-memory
-                    // footprint); an MN-major B arrives in whole 128-column boxes.
-                    mbar_arrive_expect_tx(fb, args.b_fp4  ? C::A_BYTES + C::B_BYTES / 2
-                                              : args.b_mn ? C::A_BYTES + C::B_BOXES * 128 * BK
-                                                          : C::TX_AB);
                     const int kx = (t.koff + kb) * BK;
                     const int gbz = args.mode == MODE_K_GROUPED ? 0 : t.gb;
+                    const uint32_t fb = full_bar(s);
+                    if (leader) {
+                        // An unpacking E2M1 load counts the packed bytes it reads (half its shared-memory
+                        // footprint); an MN-major B arrives in whole 128-column boxes.
+                        mbar_arrive_expect_tx(fb, args.b_fp4  ? C::A_BYTES + C::B_BYTES / 2
+                                                  : args.b_mn ? C::A_BYTES + C::B_BOXES * 128 * BK
+                                                              : C::TX_AB);
+                    }
                     if (!waited) {
                         griddep_wait();
                         waited = true;
                     }
-                    if (!args.a_mn) {
-                        tma_load_3d(base + C::OFF_A + s * C::A_BYTES, &tm_a, fb, kx, t.mb * C::TM, ga);
-                    } else {
-                        // MN-major A: one box of 128 rows x 128 K per 128-row half, 16 KB apart
+                    if (leader) {
+                        if (!args.a_mn) {
+                            tma_load_3d(base + C::OFF_A + s * C::A_BYTES, &tm_a, fb, kx, t.mb * C::TM, ga);
+                        } else {
+                            // MN-major A: one box of 128 rows x 128 K per 128-row half, 16 KB apart
 #pragma unroll
-                        for (int h = 0; h < MH; ++h)
-                            tma_load_3d(base + C::OFF_A + s * C::A_BYTES + h * (BM * BK), &tm_a, fb,
-                                        t.mb * C::TM + h * BM, kx, ga);
-                    }
-                    if (C::B_MN_OK && args.b_mn) {
-                        // MN-major B: one box of 128 columns x 128 K per 128 columns, 16 KB apart
-                        // (the descriptor's leading-dimension stride)
+                            for (int h = 0; h < MH; ++h)
+                                tma_load_3d(base + C::OFF_A + s * C::A_BYTES + h * (BM * BK), &tm_a, fb,
+                                            t.mb * C::TM + h * BM, kx, ga);
+                        }
+                        if (C::B_MN_OK && args.b_mn) {
+                            // MN-major B: one box of 128 columns x 128 K per 128 columns, 16 KB apart
+                            // (the descriptor's leading-dimension stride)
 #pragma unroll
-                        for (int j = 0; j < C::B_BOXES; ++j)
-                            tma_load_3d(base + C::OFF_B + s * C::B_STAGE + j * (128 * BK), &tm_b, fb,
-                                        t.nb * C::BN + j * 128, kx, gbz);
-                    } else {
-                        tma_load_3d(base + C::OFF_B + s * C::B_STAGE, &tm_b, fb, kx, t.nb * C::BN, gbz);
+                            for (int j = 0; j < C::B_BOXES; ++j)
+                                tma_load_3d(base + C::OFF_B + s * C::B_STAGE + j * (128 * BK), &tm_b, fb,
+                                            t.nb * C::BN + j * 128, kx, gbz);
+                        } else {
+                            tma_load_3d(base + C::OFF_B + s * C::B_STAGE, &tm_b, fb, kx, t.nb * C::BN, gbz);
+                        }
                     }
                     ++issued;
                     if (++s == C::STAGES) { s = 0; ph ^= 1u; }
@@ -771,6 +779,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     while (!mbar_try_wait(full_bar(s), ph) && global_timer_ns() - t0 < 100000000ull) {}
                 }
             }
+            __syncwarp();
         }
     } else if (warp == 1 || (C::ISSUERS == 2 && warp == C::MMA1_WARP)) {
         if constexpr (C::WG_SPLIT) setmaxnreg_dec<C::WG0_REGS>();
