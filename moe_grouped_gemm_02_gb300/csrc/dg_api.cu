@@ -226,12 +226,15 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
             // an MN-major B arrives in whole 128-column boxes
             const double b_rows = b_mn ? 128.0 * ((c->bn + 127) / 128) : c->bn;
             const double tma = 2.2 * (static_cast<double>(c->a_rows) * c->mh + b_rows);
-            // one issuer: max(161, N/2 + 33) per MMA; two issuers (MH = 2) keep the pipe at N/2 + 33;
-            // K-split issuers (KS = 2) issue two MMAs each per stage, side by side
-            const double mma = c->mh == 2   ? 8.0 * (c->bn / 2.0 + 33.0)
-                               : c->ks == 2 ? std::max(2.0 * 161.0, 4.0 * (c->bn / 2.0 + 33.0))
-                                            : 4.0 * std::max(161.0, c->bn / 2.0 + 33.0);
-            const double t_tile = kb_per * (std::max(tma, mma) + 20.0) + 3000.0 + (split > 1 ? 1500.0 : 0.0);
+            // A 128 x N x 32 MMA holds the tensor pipe N/2 cycles; the issuing loop (barrier wait and
+            // fence, commits, per-stage operands) adds to that per MMA: one issuer keeps up with
+            // no less than ~98 cycles, two K-split issuers ~74, two issuers of 128-row halves N/2.
+            const double mma = c->mh == 2   ? 8.0 * (c->bn / 2.0)
+                               : c->ks == 2 ? 4.0 * std::max(74.0, c->bn / 2.0)
+                                            : 4.0 * std::max(98.0, c->bn / 2.0);
+            // a split-K reduction (exchange and sums through distributed shared memory) costs
+            // about 2.5 us once the last stage is in
+            const double t_tile = kb_per * (std::max(tma, mma) + 20.0) + 3000.0 + (split > 1 ? 5000.0 : 0.0);
             const double cost = static_cast<double>(waves) * t_tile;
             // (within half a percent, the K-split issuers win: their stages go faster than
             // the estimate, which sees the larger of the load and MMA times only)
