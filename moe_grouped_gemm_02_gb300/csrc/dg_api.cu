@@ -234,7 +234,11 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
                                             : 4.0 * std::max(98.0, c->bn / 2.0);
             // a split-K reduction (exchange and sums through distributed shared memory) costs
             // about 2.5 us once the last stage is in
-            const double t_tile = kb_per * (std::max(tma, mma) + 20.0) + 3000.0 + (split > 1 ? 5000.0 : 0.0);
+            // loads and MMAs overlap, but not perfectly: a quarter of the shorter one shows (this
+            // separates tiles whose stages the loads bound alike, e.g. MN-major B tiles of 192 and
+            // 224 columns, which both load 256 B columns per stage)
+            const double stage = std::max(tma, mma) + 0.25 * std::min(tma, mma);
+            const double t_tile = kb_per * (stage + 20.0) + 3000.0 + (split > 1 ? 5000.0 : 0.0);
             const double cost = static_cast<double>(waves) * t_tile;
             // (within half a percent, the K-split issuers win: their stages go faster than
             // the estimate, which sees the larger of the load and MMA times only)
