@@ -160,10 +160,11 @@ bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, uint64_t elem_bytes, cons
 
 // Plan choice: a kernel configuration and a split-K factor.  The estimate, from GB300
 // measurements, is waves * (K blocks per CTA * t_kb + t_tile + t_reduce).  Per K block, an SM's
-// TMA moves about one 128-byte row per 2.2 cycles (A: 128 rows per half, B: BN rows) and a
-// 128 x N x 32 MMA costs max(161, N / 2 + 33) cycles (four per K block); t_kb is the larger.
-// A tile costs about 3000 cycles of fixed work (pipeline fill, epilogue), a split-K reduction
-// about 1500.  Waves count tiles per co-resident CTA or cluster.
+// TMA moves about one 128-byte row per 2.2 cycles (A: 128 rows per half, B: BN rows) and the
+// four 128 x N x 32 MMAs take N/2 cycles each, or what their issuing loop allows (see below);
+// t_kb is the larger plus a quarter of the smaller.  A tile costs about 3000 cycles of fixed
+// work (pipeline fill, epilogue), a split-K reduction about 5000.  Waves count tiles per
+// co-resident CTA or cluster.
 struct Plan {
     const KernelConfig* cfg = nullptr;
     int split = 1;

@@ -14,10 +14,11 @@
 //   warp 0        TMA producer: A tile [128*MH x 128 K], B tile [BN x 128 K] (128-byte swizzle;
 //                 MN-major operands in boxes of 128 MN x 128 K; E2M1 B unpacked by the TMA)
 //                 into an S-stage ring.
-//   warp 1 (+7)   MMA issuers, one lane each: kind::mxf8f6f4 block-scaled MMAs (K = 32) into
-//                 TMEM; with MH = 2 each issuer owns one 128-row half of the tile, with KS = 2
-//                 half of every stage's K steps (into its own accumulator): two instruction
-//                 streams keep the tensor pipe fed.  Warp 1 also owns TMEM.
+//   warp 1 (+7)   MMA issuers, whole warps with one elected lane issuing: kind::mxf8f6f4
+//                 block-scaled MMAs (K = 32) into TMEM; with MH = 2 each issuer owns one
+//                 128-row half of the tile, with KS = 2 half of every stage's K steps (into its
+//                 own accumulator): two instruction streams keep the tensor pipe fed.  Warp 1
+//                 also owns TMEM.
 //   warp 6        the scale warp: loads the packed scale words of every group of four K
 //                 blocks into a 2-3-slot ring as soon as a slot frees (a group ahead of the
 //                 operands) and re-lays them for tcgen05.cp.
@@ -69,11 +70,11 @@ struct GemmCfg {
     static constexpr int AR = AR_;
     static_assert(AR == 128 || (AR == 64 && MH_ == 1), "64-row A stages only with one 128-row half");
     // KS = 2: two MMA issuers split each 128-K stage (K steps 0-1 and 2-3) into the two TMEM
-    // accumulators, which the epilogue adds.  A block-scaled MMA occupies the tensor pipe for
-    // at least ~161 cycles whatever its N, so the narrow tiles of the HBM-bound shapes (N = 128,
-    // 192: 64-96 cycles of tensor work) take ~0.31 us per stage either way; the second issuer
-    // removes the issuing thread's own per-stage costs from that path (5-7 % faster decode
-    // GEMMs).  The two accumulators then serve one tile instead of alternating between tiles.
+    // accumulators, which the epilogue adds.  A block-scaled 128 x N x 32 MMA holds the tensor
+    // pipe N/2 cycles, but one issuing loop (barrier wait, fence, commits per stage) keeps up
+    // with no less than ~98 cycles per MMA; two issuers bring the narrow tiles of the
+    // HBM-bound shapes (N = 128, 192) to ~74 and N/2 cycles.  The two accumulators then serve
+    // one tile instead of alternating between tiles.
     static constexpr int KS = KS_;
     static constexpr int ISSUERS = MH * KS;
     static constexpr int ACC_ROT = KS == 2 ? 1 : ACC;   // accumulator sets rotated across tiles
