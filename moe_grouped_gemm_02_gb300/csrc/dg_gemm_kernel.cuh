@@ -900,9 +900,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // ring slot, re-lay them for tcgen05.cp, publish them to the async proxy and signal the
         // MMA issuers.  Every party uses each slot's barriers once per group, in group order, so
         // no wait is ever more than one phase from its barrier.
-        // Lane 0 also issues each group's scale loads, as soon as the group's ring slot is free
-        // (the MMAs of the group SF_SLOTS earlier are done): a whole group ahead of the A/B
-        // stages of the group, which is what hides the load latency and the re-layout.
+        // The warp also issues each group's scale loads (one elected lane), as soon as the
+        // group's ring slot is free (the MMAs of the group SF_SLOTS earlier are done): a whole
+        // group ahead of the A/B stages of the group, which is what hides the load latency and
+        // the re-layout.
+        const bool leader = elect_one_sync();
         int sf_slot = 0;
         uint32_t sff_phbits = 0;
         uint32_t sfe_phbits = 0;          // bit j: parity of scale slot j's empty barrier
@@ -916,30 +918,33 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if (t.zero) continue;
             const int ga = args.mode == MODE_MASKED ? t.g : 0;
             for (int grp = t.kb_begin >> 2; grp <= (t.kb_end - 1) >> 2; ++grp) {
-                if (lane == 0) {
-                    const uint32_t par = ((sfe_phbits >> sf_slot) & 1u) ^ 1u;
-                    if (wait_or_abort_t<C::WG_SPLIT>(sfempty_bar(sf_slot), par, misc + 1, args.err, args.timeout_ns, SITE_SF_EMPTY)) {
-                        const uint32_t sb = sffull_bar(sf_slot);
-                        mbar_arrive_expect_tx(sb, C::TX_SF);
-                        const int kp = t.kpoff + grp;
-                        if (!waited) {
-                            griddep_wait();
-                            waited = true;
-                        }
-                        tma_load_3d(base + C::OFF_SFA + sf_slot * C::SFA_BYTES, &tm_sfa, sb, t.mb * C::TM, kp, ga);
-                        tma_load_3d(base + C::OFF_SFB + sf_slot * C::SFB_BYTES, &tm_sfb, sb, t.nb * C::BN, kp,
-                                    args.mode == MODE_K_GROUPED ? 0 : t.gb);
-                        sf_last = sf_slot;
-                        sf_last_par = (sff_phbits >> sf_slot) & 1u;
-                    }
-                }
-                sfe_phbits ^= 1u << sf_slot;
-                if (__shfl_sync(0xffffffffu, misc[1], 0)) {   // aborted (lane 0's wait gave up)
+                const uint32_t par = ((sfe_phbits >> sf_slot) & 1u) ^ 1u;
+                if (!wait_fast_warp<C::WG_SPLIT>(sfempty_bar(sf_slot), par, misc + 1, args.err, args.timeout_ns,
+                                                 SITE_SF_EMPTY)) {
                     ok = false;
                     break;
                 }
-                if (!wait_fast<C::WG_SPLIT>(sffull_bar(sf_slot), (sff_phbits >> sf_slot) & 1u, misc + 1, args.err,
-                               args.timeout_ns, SITE_SF_FULL)) {
+                const uint32_t sb = sffull_bar(sf_slot);
+                if (leader) mbar_arrive_expect_tx(sb, C::TX_SF);
+                if (!waited) {
+                    griddep_wait();
+                    waited = true;
+                }
+                if (leader) {
+                    const int kp = t.kpoff + grp;
+                    tma_load_3d(base + C::OFF_SFA + sf_slot * C::SFA_BYTES, &tm_sfa, sb, t.mb * C::TM, kp, ga);
+                    tma_load_3d(base + C::OFF_SFB + sf_slot * C::SFB_BYTES, &tm_sfb, sb, t.nb * C::BN, kp,
+                                args.mode == MODE_K_GROUPED ? 0 : t.gb);
+                }
+                sf_last = sf_slot;
+                sf_last_par = (sff_phbits >> sf_slot) & 1u;
+                sfe_phbits ^= 1u << sf_slot;
+                if (__shfl_sync(0xffffffffu, misc[1], 0)) {   // another role gave up
+                    ok = false;
+                    break;
+                }
+                if (!wait_fast_warp<C::WG_SPLIT>(sffull_bar(sf_slot), (sff_phbits >> sf_slot) & 1u, misc + 1, args.err,
+                                                 args.timeout_ns, SITE_SF_FULL)) {
                     ok = false;
                     break;
                 }
@@ -952,11 +957,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 for (int c = 0; c < C::SFB_CHUNKS; ++c) relayout_sf_chunk(sfb_w + 128 * c, lane);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sfready_bar(sf_slot));
+                if (leader) mbar_arrive(sfready_bar(sf_slot));
                 if (++sf_slot == C::SF_SLOTS) sf_slot = 0;
             }
         }
-        if (lane == 0 && misc[1] && sf_last >= 0) {
+        if (leader && misc[1] && sf_last >= 0) {
             // Abort: wait (bounded, short) until the last scale load issued has landed.
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(sffull_bar(sf_last), sf_last_par) && global_timer_ns() - t0 < 100000000ull) {}
