@@ -30,7 +30,7 @@ struct DeviceState {
     int* err_ptr = nullptr;
     int max_smem = 0;   // opt-in dynamic shared memory per block
     bool prepared = false;
-    int clusters[16][3] = {};   // co-resident clusters per configuration: split 2, 4, 8 (0: unknown)
+    int clusters[16][7] = {};   // co-resident clusters per configuration and split 2..8 (0: unknown)
 };
 
 std::mutex g_mu;
@@ -184,10 +184,10 @@ int cluster_capacity(DeviceState& st, int cfg_index, const KernelConfig* c, int 
 }
 
 Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N, int kblocks, int sms,
-                 int extra_ints, int a_mn, int b_mn, int b_fp4) {
+                 int extra_ints, int a_mn, int b_mn, int b_fp4, double hbm_bytes) {
     int n = 0;
     const KernelConfig* const* cfgs = all_configs(&n);
-    // DG_FORCE_CONFIG=<name>, DG_FORCE_SPLIT=<1|2|4|8> pin the plan (tuning).
+    // DG_FORCE_CONFIG=<name>, DG_FORCE_SPLIT=<1..8> pin the plan (tuning).
     const char* force_cfg = std::getenv("DG_FORCE_CONFIG");
     const char* force_split = std::getenv("DG_FORCE_SPLIT");
     const int fsplit = force_split ? std::atoi(force_split) : 0;
@@ -196,8 +196,12 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
     for (int i = 0; i < n; ++i) {
         const KernelConfig* c = cfgs[i];
         if (force_cfg && std::strcmp(force_cfg, c->name) != 0) continue;
-        for (int split : {1, 2, 4, 8}) {
-            if (fsplit && split != fsplit) continue;
+        for (int split = 1; split <= 8; ++split) {
+            // Any split of 1..8 runs when forced; the planner itself takes 1, 2, 4 or 8: wider
+            // odd clusters measured faster as single launches but slower back to back (64x2112:
+            // split 6 8.9 vs split 4 8.5 us), where more CTAs leave fewer SMs for the next
+            // kernel's early start.
+            if (fsplit ? split != fsplit : (split & (split - 1)) != 0) continue;
             // 64-row A stages serve calls with at most 64 rows of K-major A (dense M, masked max_m)
             if (c->a_rows < 128 && (rows > c->a_rows || a_mn || (mode != MODE_DENSE && mode != MODE_MASKED)))
                 continue;
@@ -216,9 +220,7 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
             const int tma_store = split == 1 && c->smem_bytes(extra_ints, 1, 1) <= static_cast<size_t>(st.max_smem);
             int cap = sms;
             if (split > 1)
-                cap = std::min(cluster_capacity(st, i, c, split, split == 2 ? 0 : (split == 4 ? 1 : 2), split,
-                                                extra_ints),
-                               sms / split);
+                cap = std::min(cluster_capacity(st, i, c, split, split - 2, split, extra_ints), sms / split);
             if (cap <= 0) continue;
             const long long m_units = c->mh == 2 ? (m_blocks_total + 1) / 2 : m_blocks_total;
             const long long tiles = m_units * ((N + c->bn - 1) / c->bn);
@@ -239,8 +241,11 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
             // separates tiles whose stages the loads bound alike, e.g. MN-major B tiles of 192 and
             // 224 columns, which both load 256 B columns per stage)
             const double stage = std::max(tma, mma) + 0.25 * std::min(tma, mma);
-            const double t_tile = kb_per * (stage + 20.0) + 3000.0 + (split > 1 ? 5000.0 : 0.0);
-            const double cost = static_cast<double>(waves) * t_tile;
+            const double fixed = 3000.0 + (split > 1 ? 5000.0 : 0.0);
+            const double t_tile = kb_per * (stage + 20.0) + fixed;
+            // however the work is spread, the operands cross HBM at ~6.2 TB/s (~3000 bytes per
+            // cycle at 2.07 GHz)
+            const double cost = std::max(static_cast<double>(waves) * t_tile, hbm_bytes / 3000.0 + fixed);
             // (within half a percent, the K-split issuers win: their stages go faster than
             // the estimate, which sees the larger of the load and MMA times only)
             const bool better = !best.cfg || cost < best_cost * 0.995 ||
@@ -354,8 +359,12 @@ dg_status run_gemm(const GemmCall& call, void* stream) {
     // Kb / 4 + G rows in all (each group rounds its own count up).
     const int plan_kb = kgrouped ? std::max(1, (Kb + groups - 1) / groups) : Kb;
     const int kp_rows = kgrouped ? Kb / 4 + groups : Kp;
-    const Plan plan =
-        choose_plan(*st, mode, rows, m_blocks * groups, N, plan_kb, sms, extra_ints, call.a_mn, call.b_mn, call.b_fp4);
+    // the operands' bytes (A as stored, B of every group, half for E2M1): what the GEMM reads
+    // from HBM at least
+    const double hbm_bytes = static_cast<double>(rows) * (mode == MODE_MASKED ? groups : 1) * K +
+                             static_cast<double>(kgrouped ? 1 : call.b_groups) * N * K * (call.b_fp4 ? 0.5 : 1.0);
+    const Plan plan = choose_plan(*st, mode, rows, m_blocks * groups, N, plan_kb, sms, extra_ints, call.a_mn,
+                                  call.b_mn, call.b_fp4, hbm_bytes);
     if (!plan.cfg) return DG_ERR_SHAPE;   // nothing fits in shared memory (too many groups)
     const KernelConfig* cfg = plan.cfg;
 

@@ -140,14 +140,14 @@ struct GemmCfg {
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort flag
     static constexpr int OFF_CUM = OFF_MISC + 16;             // masked mode: m-unit prefix sums
     // Split-K receive buffer: one slot per other CTA of the cluster, each holding the (at most
-    // AR / split) rows this CTA owns, BN FP32 per row (rows padded by 16 bytes).
+    // ceil(AR / split)) rows this CTA owns, BN FP32 per row (rows padded by 16 bytes).
     static constexpr int RECV_ROW = BN * 4 + 16;
     static __host__ __device__ uint32_t off_recv(int extra_ints) {
         return (static_cast<uint32_t>(OFF_CUM + extra_ints * 4) + 15u) & ~15u;
     }
     static_assert(128 * RECV_ROW <= OFF_SFA, "split-K staging of a whole tile fits in the operand ring");
     static __host__ __device__ uint32_t recv_bytes(int split) {
-        return split > 1 ? static_cast<uint32_t>((split - 1) * (AR / split) * RECV_ROW) : 0u;
+        return split > 1 ? static_cast<uint32_t>((split - 1) * ((AR + split - 1) / split) * RECV_ROW) : 0u;
     }
     // Without split-K the space after the prefix sums stages the epilogue's output boxes: two
     // 1 KB buffers per epilogue warp (32 rows x 32 bytes each), the source of TMA bulk stores,
@@ -1044,7 +1044,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 const uint32_t V = static_cast<uint32_t>(min(C::AR, max(0, m_valid - t.mb * BM)));
                 const uint32_t usplit = static_cast<uint32_t>(split);
                 const uint32_t RPO = V > 0 ? (V + usplit - 1) / usplit : 1u;
-                const uint32_t RPO_CAP = C::AR / usplit;             // rows of a receive slot
+                const uint32_t RPO_CAP = (C::AR + usplit - 1) / usplit;   // rows of a receive slot
                 const uint32_t r_in_tile = q * 32u + lane;
                 const bool valid_row = r_in_tile < V;
                 const uint32_t owner = valid_row ? r_in_tile / RPO : crank;

@@ -60,7 +60,7 @@ def test_dense_every_plan(cfg, split, few_sms, monkeypatch):
     assert_within_tolerance(bits(d), want, f"{cfg} split {split}")
 
 
-@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("split", [2, 3, 4, 5, 6, 8])
 def test_split_k_decode_shape(split, monkeypatch):
     monkeypatch.setenv("DG_FORCE_SPLIT", str(split))
     M, N, K = 64, 2112, 7168
@@ -75,7 +75,7 @@ def test_split_k_decode_shape(split, monkeypatch):
 
 @pytest.mark.parametrize("cfg", ["config_bn128_s8_k2_r64"])
 @pytest.mark.parametrize("M", [1, 37, 64])
-@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("split", [1, 2, 3, 4, 6, 8])
 def test_64_row_a_stages(cfg, M, split, few_sms, monkeypatch):
     # The configurations that load only 64 rows of A per stage (their MMAs still read 128 rows,
     # the upper 64 from the next buffer): dense calls of at most 64 rows, on a few SMs so that
@@ -173,10 +173,11 @@ def test_contiguous_256_row_tiles_straddling_experts(cfg, few_sms, monkeypatch):
 
 
 @pytest.mark.parametrize("cfg", ["config_bn128_s4_a2", "config_bn64_s8_a2", "config_bn32_s8_a2"])
-@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("split", [2, 3, 4, 5, 6, 7, 8])
 def test_split_k_rows_per_owner(cfg, split, few_sms, monkeypatch):
-    # 128 / split rows of each tile per owning CTA (64, 32, 16); 36 K blocks = 9 groups, so the
-    # 8-way split has uneven K ranges; ragged M and N.
+    # ceil(V / split) rows of each tile's V valid rows per owning CTA (64, 43, 32, 26, 22, 19 and
+    # 16 of a full 128-row tile; the last owner takes fewer); 36 K blocks = 9 groups, so most
+    # splits have uneven K ranges; ragged M and N.
     monkeypatch.setenv("DG_FORCE_CONFIG", cfg)
     monkeypatch.setenv("DG_FORCE_SPLIT", str(split))
     M, N, K = 200, 448, 4608

@@ -98,7 +98,7 @@ def run_protocol(split, units, seed, *, unit_done_wait=True, local_arrivals=True
             last_unit = u == last_any
             row_bytes = recv_row if last_unit else bn
             rpo = (V + split - 1) // split
-            cap = 128 // split
+            cap = (128 + split - 1) // split
             q0 = 32 * q
             own0 = min(V, c * rpo)
             own1 = min(V, own0 + rpo)
@@ -203,7 +203,7 @@ def run_protocol(split, units, seed, *, unit_done_wait=True, local_arrivals=True
 def _cases(n, seed0):
     rng = random.Random(seed0)
     for i in range(n):
-        split = rng.choice([2, 4, 8])
+        split = rng.randint(2, 8)
         units = [rng.choice([0, 1, 2, 17, 31, 32, 33, 64, 71, 100, 127, 128, rng.randint(1, 128)])
                  for _ in range(rng.randint(1, 7))]
         yield i, split, units
