@@ -38,7 +38,8 @@
  *    accumulator).
  *  - The environment variable DG_PRINT_CONFIGS=1 prints the kernel configuration chosen
  *    for each call to stderr; DG_NUM_SMS=n caps the SMs used (as dg_set_num_sms).
- *    DG_FORCE_CONFIG / DG_FORCE_SPLIT pin the kernel plan (tuning and tests);
+ *    DG_FORCE_CONFIG=<configuration name> / DG_FORCE_SPLIT=<1..8> pin the kernel plan
+ *    (tuning and tests; the planner itself splits K over 1, 2, 4 or 8 CTAs);
  *    DG_TIMEOUT_MS sets the bound on each in-kernel barrier wait (default 4000) and
  *    DG_DEBUG_DROP_LOAD=n makes the GEMM skip its n-th load stage, so that a wait runs out:
  *    a test hook for the timeout path (dg_check_device_error then reports DG_ERR_TIMEOUT).
