@@ -3,8 +3,8 @@
 Each case drives one index of the kernels far past the bench's shapes: a K of 65536 (512
 K blocks per output tile, 128 packed scale words per row), N = 131136 (1025 column tiles of
 128, an N tail of 64), 4096 masked groups (the library's maximum: the device-side prefix over
-the groups is at its largest) and a contiguous call over 256 experts, most of them empty or
-ragged.  Results are checked element by element against the oracle; rows the layouts must not
+the groups is at its largest), a contiguous call over 256 experts, many of them empty, a
+K-grouped call over 64 ragged or empty groups, and E2M1 weights over 256 K blocks.  Results are checked element by element against the oracle; rows the layouts must not
 touch are checked bit-exactly.
 """
 import numpy as np
@@ -80,3 +80,35 @@ def test_many_contiguous_experts():
     want = oracle.m_grouped_fp8_gemm_nt_contiguous(w["a"], sfa, w["b"], sfb, w["m_indices"])
     assert np.all(got[~valid] == 0), "padding rows must be +0.0"
     assert_within_tolerance(got[valid], want[valid], "256 experts")
+
+
+def test_k_grouped_many_groups():
+    # 64 expert gradients, their K (token) ranges ragged, a quarter of them empty.
+    from tests._parity import assert_close_f32
+    G, M, N = 64, 128, 256
+    ks = (synth.rng(85, "counts").integers(0, 6, size=G) * 128).astype(np.int64)
+    ks[synth.rng(85, "counts", sub=1).random(G) < 0.25] = 0
+    w = synth.make_k_grouped(M, N, ks, seed=85)
+    sfa = oracle.pack_sf_ue8m0_k_grouped(w["sfa"], M, ks)
+    sfb = oracle.pack_sf_ue8m0_k_grouped(w["sfb"], N, ks)
+    d = torch.full((G, M, N), float("nan"), dtype=torch.float32, device="cuda")
+    dg.dg_k_grouped_fp8_gemm_tn_contiguous(to_dev(w["a"]), to_dev(sfa), to_dev(w["b"]), to_dev(sfb), d,
+                                           to_dev(ks.astype(np.int32)))
+    dg.dg_check_device_error()
+    got = d.cpu().numpy()
+    want = oracle.k_grouped_fp8_gemm_tn_contiguous(w["a"], sfa, w["b"], sfb, ks)
+    assert_close_f32(got, want, "64 K groups")
+    for g in np.nonzero(ks == 0)[0]:
+        assert np.all(got[g] == 0) and not np.any(np.signbit(got[g]))
+
+
+def test_fp8_fp4_long_k():
+    # E2M1 weights over 256 K blocks (64 packed scale words per row).
+    M, N, K = 64, 512, 32768
+    w = synth.with_fp4_b(synth.make_dense(M, N, K, seed=86), seed=86)
+    sfa = oracle.pack_sf_ue8m0(w["sfa"], M, 1)[0]
+    sfb = oracle.pack_sf_ue8m0(w["sfb_fp4"], N, 1)[0]
+    d = torch.full((M, N), SENT, dtype=torch.int16, device="cuda")
+    dg.dg_fp8_fp4_gemm_nt(to_dev(w["a"]), to_dev(sfa), to_dev(w["b_fp4"]), to_dev(sfb), d)
+    dg.dg_check_device_error()
+    assert_within_tolerance(bits(d), oracle.fp8_fp4_gemm_nt(w["a"], sfa, w["b_fp4"], sfb), "fp8xfp4 K = 32768")
