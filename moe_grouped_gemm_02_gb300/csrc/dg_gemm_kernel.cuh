@@ -999,6 +999,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // peers' partial rows have landed here, so that the barrier's latency overlaps the sums
         // and stores; it only waits at exit)
         bool final_arrived = false;
+        bool first_red = true;   // split-K: no unit of this CTA reduced yet
         for (int u = u_first; u < total_units; u += u_step) {
             if (misc[1]) break;
             const Unit t = decode_unit<MH>(args, cum, u, kb0, kb1);
@@ -1062,13 +1063,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                 if (!wait_or_abort_t<C::WG_SPLIT>(tfull_bar(acc), acc_ph, misc + 1, args.err, args.timeout_ns, SITE_TMEM_FULL)) break;
                 tc_fence_after_sync();
                 const uint32_t t_row = tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(acc * C::ACC_STRIDE);
-                // the other CTAs are done with the previous unit's receive slots
+                // The other CTAs are done with the previous unit's receive slots.  On this CTA's
+                // first unit there is no previous unit: the waits (for the phase before the
+                // barriers' first) would pass at once, and are skipped, because each cluster-scope
+                // acquire costs a few hundred cycles even then (measured ~0.5 us for three, on
+                // the critical path of a one-unit decode GEMM).
                 bool slots_free = true;
-                for (uint32_t o = 0; o < usplit && slots_free; ++o)
+                for (uint32_t o = 0; o < usplit && slots_free && !first_red; ++o)
                     if (o != crank)
                         slots_free = wait_cluster_or_abort_t<C::WG_SPLIT>(slotfree_bar(o), red_eph ^ 1u, misc + 1, args.err,
                                                            args.timeout_ns, SITE_RED_EMPTY);
                 if (!slots_free) break;
+                first_red = false;
                 red_eph ^= 1u;
                 __syncwarp();
                 if (lane == 0)
@@ -1135,8 +1141,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     for (uint32_t qq = qr0; qq < qr1; ++qq) red_fmask ^= 1u << qq;
                     // Everything the peers send here has landed, and the peers arrive only once
                     // this CTA's rows have landed there: the final barrier may count this warp.
+                    // The arrival needs no release: what it guards (no CTA leaves while a peer's
+                    // copy or remote arrival may still reach its shared memory) is already ordered
+                    // by the receive barriers.  Every copy into or out of this CTA completes on a
+                    // receive barrier that its receiver waits for before arriving, and each
+                    // slot-free arrival of an earlier unit was observed by its receiver before that
+                    // CTA sent the data this warp has just waited for.  (A release arrival measured
+                    // ~0.2 us later.)
                     __syncwarp();
-                    cluster_arrive();
+                    cluster_arrive_relaxed();
                     final_arrived = true;
                     constexpr uint32_t UPR = C::BN / 8;               // 16-byte units per row
                     const uint32_t et = (warp - C::EPI0) * 32u + lane;  // epilogue thread 0..127

@@ -113,8 +113,9 @@ __device__ __forceinline__ void cluster_sync_all() {
 __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
-// Arrival without release semantics: for a thread whose only writes the peers rely on are
-// mbarrier initialisations it has already published with fence.mbarrier_init.release.cluster.
+// Arrival without release semantics: for a thread whose writes the peers rely on are already
+// ordered otherwise (mbarrier initialisations published with fence.mbarrier_init.release.cluster,
+// or copies whose completion the peers have waited for on their own barriers).
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
