@@ -96,17 +96,28 @@ def _check(call: str, status: int) -> None:
         raise DGError(call, status)
 
 
-def _ptr(t: torch.Tensor, what: str) -> ctypes.c_void_p:
+# The pointer and stream arguments go to ctypes as plain integers (the argument types above
+# convert them): a call's marshalling then costs a few microseconds, less than the decode-size
+# GEMMs it launches.  The current stream comes from torch's raw accessor where it has one
+# (torch.cuda.current_stream() builds a Stream object, ~3 us per call).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
+def _ptr(t: torch.Tensor, what: str) -> int:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{what} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{what} must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
-def _stream(stream) -> ctypes.c_void_p:
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+def _stream(stream) -> int:
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None and _cur_device is not None:
+        return _raw_stream(_cur_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def dg_get_mk_alignment_for_contiguous_layout() -> int:
