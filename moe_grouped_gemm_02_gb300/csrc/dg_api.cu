@@ -235,12 +235,14 @@ Plan choose_plan(DeviceState& st, int mode, int rows, int m_blocks_total, int N,
             const double mma = c->mh == 2   ? 8.0 * (c->bn / 2.0)
                                : c->ks == 2 ? 4.0 * std::max(74.0, c->bn / 2.0)
                                             : 4.0 * std::max(98.0, c->bn / 2.0);
-            // a split-K reduction (exchange and sums through distributed shared memory) costs
-            // about 2.5 us once the last stage is in
             // loads and MMAs overlap, but not perfectly: a quarter of the shorter one shows (this
             // separates tiles whose stages the loads bound alike, e.g. MN-major B tiles of 192 and
             // 224 columns, which both load 256 B columns per stage)
             const double stage = std::max(tma, mma) + 0.25 * std::min(tma, mma);
+            // per tile: start and epilogue ~3000 cycles; a split-K reduction (exchange and sums
+            // through distributed shared memory) ~1.7 us more once the last stage is in.  The
+            // 5000 cycles were fitted when it took ~2.4 us; re-measured since, the plans they pick
+            // (split 4 for the M = 64 decode shapes, none for M = 128) are still the fastest.
             const double fixed = 3000.0 + (split > 1 ? 5000.0 : 0.0);
             const double t_tile = kb_per * (stage + 20.0) + fixed;
             // however the work is spread, the operands cross HBM at ~6.2 TB/s (~3000 bytes per
