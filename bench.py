@@ -860,7 +860,8 @@ def time_oracle(ws, budget_s: float = 20.0, rows_per_workload: int = 4):
             oracle.m_grouped_fp8_gemm_nt_contiguous(w["a"], sfa, w["b"], sfb, w["m_indices"], rows=rows)
             n_rows = len(rows)
         else:
-            mm = np.minimum(w["masked_m"], 1)      # one valid row per group
+            # the first rows of each group, about rows_per_workload in all
+            mm = np.minimum(w["masked_m"], max(1, rows_per_workload // w["G"]))
             sfa = oracle.pack_sf_ue8m0(w["sfa"], w["max_m"], 1)
             sfb = oracle.pack_sf_ue8m0(w["sfb"], N, 128)
             prior = np.zeros((w["G"], w["max_m"], N), np.uint16)
@@ -875,18 +876,29 @@ def time_oracle(ws, budget_s: float = 20.0, rows_per_workload: int = 4):
             "seconds": round(t_total, 2)}
 
 
+REFERENCE_BUDGET_S = 150.0   # the whole --impl reference run (warm-up and timed steps)
+
+
 def run_reference(args, rank: int, world: int):
-    """The oracle timed as it stands: each step is a bounded sample of the suite."""
+    """The oracle timed as it stands: each step is a bounded sample of the suite.  The sample
+    (output rows per workload, the same for every step) is sized from two timed warm-up passes
+    so that all warm-up and timed steps together take about REFERENCE_BUDGET_S: each oracle
+    call decodes the whole weight matrix, so a one-row sample would time mostly that decode."""
     if rank != 0:
         return None
     ws = make_workloads(seed=0)
+    t_1 = time_oracle(ws, budget_s=1e9, rows_per_workload=1)["seconds"]
+    t_16 = time_oracle(ws, budget_s=1e9, rows_per_workload=16)["seconds"]
+    per_row = max(t_16 - t_1, 1e-3) / 15.0
+    per_step = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(1024, (per_step - t_1) / per_row)))
     for _ in range(args.warmup):
-        time_oracle(ws, budget_s=1e9, rows_per_workload=1)
+        time_oracle(ws, budget_s=1e9, rows_per_workload=rows)
     vals = []
     t0 = time.perf_counter()
     flops = 0.0
     for _ in range(args.steps):
-        r = time_oracle(ws, budget_s=1e9, rows_per_workload=1)
+        r = time_oracle(ws, budget_s=1e9, rows_per_workload=rows)
         vals.append(r)
     elapsed = time.perf_counter() - t0
     value = statistics.mean(v["value"] for v in vals)
