@@ -83,12 +83,17 @@ struct GemmCfg {
     // and 4 more epilogue warps, one set per 128-row half (MH = 2)
     // With one 128-row half and one accumulator, the MMAs of the next tile wait for the
     // epilogue to drain TMEM: two sets of four epilogue warps then split the tile's columns.
-    static constexpr int EPI_COLS = (MH == 1 && ACC_ == 1 && BN_ % 64 == 0) ? 2 : 1;
+    // So do K-split tiles wider than 128 columns: their epilogue reads two accumulators, and
+    // with a whole row per thread it had registers for 16 columns per TMEM round trip only
+    // (12 round trips for 192 columns, ~0.1 us each, on the critical path of every decode
+    // launch); with half a row per thread it loads 32 at a time (3 round trips).
+    static constexpr int EPI_COLS =
+        (MH == 1 && BN_ % 64 == 0 && (ACC_ == 1 || (KS_ == 2 && BN_ > 128))) ? 2 : 1;
     static constexpr int THREADS = (MH == 2 || EPI_COLS == 2) ? 384 : (KS == 2 ? 256 : 224);
     static constexpr int EPI_THREADS = 128 * MH * EPI_COLS;
     // Warp roles.  224/256 threads: producer 0, MMA issuer 1 (and 7 with KS = 2), epilogue 2-5,
     // scale warp 6.  384 threads (two sets of epilogue warps): warpgroup 0 holds the producer
-    // (0), the issuers (1, and 3 with MH = 2) and the scale warp (2); warpgroups 1 and 2 the
+    // (0), the issuers (1, and 3 with MH = 2 or KS = 2) and the scale warp (2); warpgroups 1 and 2 the
     // epilogue warps (4-7, 8-11).  Registers are then re-split per warpgroup (setmaxnreg):
     // the launch gives every thread 168, warpgroup 0 drops to WG0_REGS and the epilogue
     // warpgroups rise to EPI_REGS, which holds a 208-column BF16 row with no spills.
@@ -1369,11 +1374,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                     // them, instead of after a chain of row stores.  Masked slabs that reach past
                     // masked_m keep the row stores below (rows past it stay untouched).
                     const bool last_unit_here = u + u_step >= total_units;
-                    if (C::ACC == 2 && args.tma_store && slab_tma && last_unit_here && C::BN % 64 == 0) {
-                        const uint32_t region = base + C::OFF_A + ew * static_cast<uint32_t>(32 * C::BN * 2);
+                    constexpr int SEG = C::BN / C::EPI_COLS;     // this warp's columns of the tile
+                    if (C::ACC == 2 && args.tma_store && slab_tma && last_unit_here && SEG % 64 == 0) {
+                        const uint32_t region = base + C::OFF_A + ew * static_cast<uint32_t>(32 * SEG * 2);
                         const uint32_t rsw = lane & 7u;
 #pragma unroll
-                        for (int b = 0; b < C::BN / 64; ++b) {
+                        for (int b = 0; b < SEG / 64; ++b) {
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
                                 const uint32_t* p = pk + 8 * (4 * b + j / 2) + 4 * (j % 2);
@@ -1385,9 +1391,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
-                            for (int b = 0; b < C::BN / 64; ++b)
-                                if (n0 + 64 * b < N)
-                                    tma_store_3d(&tm_d64, region + static_cast<uint32_t>(b) * 4096u, n0 + 64 * b, slab0, t.g);
+                            for (int b = 0; b < SEG / 64; ++b)
+                                if (n0 + 32 * ch_lo + 64 * b < N)
+                                    tma_store_3d(&tm_d64, region + static_cast<uint32_t>(b) * 4096u, n0 + 32 * ch_lo + 64 * b,
+                                                 slab0, t.g);
                             bulk_commit_group();
                         }
                         ++nbox;
